@@ -1,0 +1,396 @@
+"""Benchmark: one batched owner-side Muon step per timed step, on synthetic
+LLM-shaped matrix sets (default: the Llama-3.1-8B projection set, 224
+matrices, bf16 weights and grads, fp32 momentum, ns_steps=5).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line. ``value`` is the algorithmic Newton-Schulz throughput
+(TFLOP/s, symmetric products counted once) over the whole step time
+(momentum pass + Newton-Schulz + update) for all ranks together; ``ms_per_step``
+is the step time. With N > 1 (torchrun) each rank runs its own replica of the
+matrix set (independent matrices, no collective on the data path): weak
+scaling; the time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle instead (on the host cores, a
+bounded sample of the same workload per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms & NS TFLOP/s (% of GB300 bf16 peak) per model matrix set, 1 GPU"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "gemm": ["tc_ns.cu", "ptx.cuh", "internal.h"],
+    "gram": ["tc_ns.cu", "ptx.cuh", "internal.h"],
+    "poly": ["tc_ns.cu", "ptx.cuh", "internal.h"],
+    "momentum": ["momentum.cu", "internal.h"],
+}
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def replica_seed_offset(rank: int) -> int:
+    """Each rank draws its own replica of the matrix set."""
+    return 100_000 * rank
+
+
+def aggregate(flops_per_step_per_rank: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: all ranks' work divided by the slowest rank's time."""
+    return flops_per_step_per_rank * steps * world / max_seconds / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kind, []):
+        with open(os.path.join(ROOT, "matrix_optimizer_update_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kind: str, workload: str):
+    """DRAM bytes per launch of ``kind`` from the committed ncu summary, or None
+    when there is none for this workload or the kernel source changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload, {}).get(kind)
+    if not e or e.get("source_sha") != kernel_source_sha(kind):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(workload, budget_s: float, start_layer: int = 0, max_mats=None):
+    """Time the fp64 oracle on whole matrices of the workload, in layer order,
+    until ``budget_s`` is spent. Returns (seconds, algorithmic NS flops, names)."""
+    import numpy as np
+
+    from matrix_optimizer_update_gb300 import workloads as wl
+    from oracle import muon_ref as ref
+
+    rng = np.random.default_rng(12345)
+    done_flops, names, spent = 0, [], 0.0
+    for li, (layer, role, r, c, e) in enumerate(workload.matrices()):
+        if layer < start_layer:
+            continue
+        G = rng.standard_normal((r, c)) * workload.grad_std
+        W = rng.standard_normal((r, c)) * workload.weight_std
+        M = np.zeros((r, c))
+        t0 = time.perf_counter()
+        ref.muon_step(W, G, M, lr=workload.lr, mu=workload.mu, nesterov=workload.nesterov,
+                      ns_steps=workload.ns_steps, coeffs=workload.coeffs, eps=workload.eps)
+        spent += time.perf_counter() - t0
+        done_flops += wl.ns_flops(r, c, workload.ns_steps)
+        names.append(f"L{layer}.{role}" + (f".e{e}" if e >= 0 else "") + f" {r}x{c}")
+        if spent >= budget_s or (max_mats is not None and len(names) >= max_mats):
+            break
+    return spent, done_flops, names
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from matrix_optimizer_update_gb300 import workloads as wl
+
+    w = wl.get(args.workload)
+    # per step: the first matrices of the set in layer order, bounded to ~4 s of CPU work
+    per_step_budget = 4.0
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, max_mats=1)
+    total_s, total_f, names = 0.0, 0, []
+    for k in range(args.steps):
+        s, f, nm = oracle_sample(w, per_step_budget)
+        total_s += s
+        total_f += f
+        names = nm
+    value = total_f / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "matrices": len(w.shapes), "sample_per_step": names},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"per step: {', '.join(names)} (fp64 numpy oracle, whole matrices)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    from matrix_optimizer_update_gb300 import build as build_mod
+    from matrix_optimizer_update_gb300 import dmuon as dm
+    from matrix_optimizer_update_gb300 import workloads as wl
+    from matrix_optimizer_update_gb300.inputs import make_matrix_set
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    build_mod.build()
+    w = wl.get(args.workload)
+    tot = wl.totals(w)
+    ms = make_matrix_set(w, f"cuda:{local}", seed_offset=replica_seed_offset(rank))
+    stream = torch.cuda.Stream()
+    muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
+                          grad=w.grad_dtype, compute=w.compute, device=f"cuda:{local}", stream=stream)
+    plan = muon.plan
+    desc = plan.describe()
+    launches_per_step = len(desc["launches"])
+    Wp, Gp, Mp = ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M)
+    sh = stream.cuda_stream
+
+    def step():
+        plan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    barrier()
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    plan.profile_begin(args.steps * launches_per_step)
+    c0 = plan.launch_count()
+    torch.cuda.synchronize()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = plan.launch_count() - c0
+    prof = plan.profile_end(args.steps * launches_per_step)
+    clk = clocks.stop()
+    status = plan.read_device_status(sh)
+
+    max_ms = elapsed_ms
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([elapsed_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    # ---- per-kind accounting from the live events
+    per_kind = {}
+    for kind, kms, work in prof:
+        d = per_kind.setdefault(dm.KIND_NAMES[kind], {"ms": 0.0, "work": 0.0, "launches": 0})
+        d["ms"] += kms
+        d["work"] += work
+        d["launches"] += 1
+    ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in ("gram", "poly", "gemm")) / args.steps
+    peaks, peak_src = load_peaks()
+    tensor_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ns_kinds = {k: v for k, v in per_kind.items() if k in ("gram", "poly", "gemm")}
+    dom = max(ns_kinds, key=lambda k: ns_kinds[k]["ms"]) if ns_kinds else max(per_kind, key=lambda k: per_kind[k]["ms"])
+    d = per_kind[dom]
+    if dom in ("gram", "poly", "gemm"):
+        achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak, "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
+                "traffic": traffic_for(dom, w.name)}
+    else:
+        achieved = d["work"] / (d["ms"] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
+                "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
+                "traffic": traffic_for(dom, w.name)}
+    kernels = {}
+    for k, v in per_kind.items():
+        if k in ("gram", "poly", "gemm"):
+            a = v["work"] / (v["ms"] * 1e-3) / 1e12
+            kernels[k] = {"ms_per_step": v["ms"] / args.steps, "tflops": a, "frac_of_tensor_peak": a / tensor_peak}
+        else:
+            a = v["work"] / (v["ms"] * 1e-3) / 1e9
+            kernels[k] = {"ms_per_step": v["ms"] / args.steps, "gbs": a, "frac_of_hbm_peak": a / hbm_peak,
+                          "traffic": traffic_for(k, w.name)}
+
+    # ---- end to end: grads in from pinned host memory, updated weights out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(2, min(args.steps, 5))
+        hG = torch.empty_like(ms.G, device="cpu", pin_memory=True)
+        hW = torch.empty_like(ms.W, device="cpu", pin_memory=True)
+        hG.copy_(ms.G)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(e2e_steps):
+                ms.G.copy_(hG, non_blocking=True)
+                step()
+                hW.copy_(ms.W, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([e2e_ms], device=f"cuda:{local}")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
+               "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+               "h2d_bytes_per_step": hG.numel() * hG.element_size(),
+               "d2h_bytes_per_step": hW.numel() * hW.element_size()}
+        del hG, hW
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s, f, names = oracle_sample(w, args.cpu_budget)
+        cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{len(names)} whole matrices of layer 0 in order ({'; '.join(names)}), fp64 numpy, "
+                         f"{s:.1f} s"}
+
+    value = aggregate(tot["ns_flops"], args.steps, world, max_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.compute == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "matrices": tot["matrices"], "params": tot["params"],
+                   "ns_steps": w.ns_steps, "ns_flops_per_step": tot["ns_flops"],
+                   "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
+        "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
+        "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
+        "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk, "device_status": status,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama-3.1-8b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

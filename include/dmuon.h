@@ -1,0 +1,225 @@
+/*
+ * dmuon.h - C ABI of the owner-side batched Muon update on one GB300 GPU.
+ *
+ * The library runs, for a whole batch of 2-D weight matrices in one pass, the
+ * update that a DMuon owner performs on the matrices it owns ("DMuon:
+ * Efficient Distributed Muon Training with Near-Adam Overhead", gist.science
+ * technical summary, section 2.1 "Owner-Centric Executiestrategie": the owner
+ * keeps the optimizer state and runs the Newton-Schulz iteration and the
+ * update once per matrix; section 1 "Probleemstelling": Newton-Schulz on the
+ * momentum-aggregated gradient, built on the product X X^T). Per matrix W
+ * (rows x cols, row-major, rows = dim 0), gradient G and momentum M:
+ *
+ *   M  <- mu*M + G;   U = G + mu*M (Nesterov) or U = M
+ *   X  <- U / (||U||_F + eps), transposed when rows > cols (short side first)
+ *   repeat ns_steps:  A = X X^T;  B = b*A + c*A*A;  X <- a*X + B*X
+ *   W  <- W - lr * sqrt(max(1, rows/cols)) * X     (X back in W's orientation)
+ *
+ * The two calls follow the problem statement of the pages: a plan built once
+ * from the list of matrix shapes, the Newton-Schulz step count, coefficients
+ * and dtypes ("dmuon_plan"), and a step taking params, grads and momenta
+ * ("dmuon_step"). Matrices of equal shape are batched into one bucket and
+ * every phase runs all buckets in one launch (summary section 2,
+ * "Batching"); tiles are ordered by computational cost, largest first, the
+ * greedy fallback of the cost-based balancing in summary section 2.3.
+ *
+ * Conventions for every entry point:
+ *  - Every call returns a dmuon_status; nothing else crosses the ABI. On an
+ *    error, dmuon_last_error() returns a message (thread-local, valid until
+ *    the next call on the same thread).
+ *  - Argument errors are detected on the host before anything is launched.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Device pointers must address memory of the current CUDA device.
+ *  - The library never allocates device memory: the caller owns the
+ *    workspace and every parameter, gradient and momentum buffer.
+ *  - Device-detected conditions (non-finite norm, a pipeline wait that ran
+ *    out of time) are bits of a status word in the workspace, never traps;
+ *    read them with dmuon_read_device_status().
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DMUON_OK = 0,
+  DMUON_ERR_INVALID_ARG = -1, /* bad shape, count, pointer, size or value      */
+  DMUON_ERR_UNSUPPORTED = -2, /* dtype combination or flag not supported       */
+  DMUON_ERR_WORKSPACE = -3,   /* workspace NULL, too small or misaligned       */
+  DMUON_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed             */
+  DMUON_ERR_NOT_BOUND = -5,   /* dmuon_step before dmuon_plan_bind             */
+  DMUON_ERR_DEVICE = -6       /* a device status bit is set (see below)        */
+} dmuon_status;
+
+typedef enum { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
+
+/* Stored shape of one matrix: rows = dim 0, row-major, contiguous. */
+typedef struct {
+  int64_t rows;
+  int64_t cols;
+} dmuon_shape;
+
+/* Storage dtypes of the step's tensors and the arithmetic mode.
+ *   param:    DMUON_F32 or DMUON_BF16 (weights, updated in place)
+ *   grad:     DMUON_F32 or DMUON_BF16 (read only)
+ *   momentum: DMUON_F32 only (updated in place)
+ *   compute:  DMUON_F32  = fp32 operands and fp32 accumulation everywhere;
+ *             DMUON_BF16 = bf16 Newton-Schulz operands (X, A, B stored bf16)
+ *                          with fp32 accumulation on the tensor cores.      */
+typedef struct {
+  int32_t param;
+  int32_t grad;
+  int32_t momentum;
+  int32_t compute;
+} dmuon_dtypes;
+
+/* Plan flags. */
+#define DMUON_FLAG_CAPTURE_UPDATE 0x1u /* keep the fp32 update X of the last step
+                                          (read it with dmuon_read_update)      */
+
+/* Device status bits (dmuon_read_device_status). */
+#define DMUON_DEV_NONFINITE_NORM 0x1u  /* ||U||_F was NaN or Inf for some matrix  */
+#define DMUON_DEV_WAIT_TIMEOUT 0x2u    /* a pipeline wait ran out of time; the
+                                          kernel returned early, results invalid */
+
+/* Launch kinds reported by the profiler. */
+#define DMUON_KIND_MOMENTUM 0 /* momentum + sum of squares + cast/transposed copy */
+#define DMUON_KIND_GRAM 1     /* A = X X^T, upper tiles, mirrored                  */
+#define DMUON_KIND_POLY 2     /* B = b*A + c*A A^T, upper tiles, mirrored          */
+#define DMUON_KIND_GEMM 3     /* X' = a*X + B X (last step: W update epilogue)     */
+#define DMUON_KIND_UPDATE0 4  /* W update straight from U (ns_steps == 0)          */
+
+typedef struct dmuon_plan_s* dmuon_plan_t;
+
+/*
+ * dmuon_plan - validate a batch description and build the host-side plan.
+ *
+ *  shapes[n_mats]     stored shape of each matrix; 1 <= rows, cols <= 2^20 and
+ *                     rows*cols < 2^31.
+ *  ns_steps           number of Newton-Schulz steps, 0..16.
+ *  coeffs             host array of 3*n_coeff_triples floats (a, b, c, ...);
+ *                     n_coeff_triples is 1 (same triple every step) or
+ *                     ns_steps (one triple per step). NULL with 0 triples
+ *                     selects (3.4445, -4.7750, 2.0315).
+ *  eps                added to the Frobenius norm (not its square); >= 0.
+ *  dtypes, flags      see above. momentum must be DMUON_F32.
+ *  out                receives the plan handle (host memory, owned by the
+ *                     library until dmuon_plan_destroy).
+ *
+ * Needs no GPU: only host memory is touched. Matrices with equal (short, long)
+ * shape share a bucket; per phase the tiles of all buckets are listed and
+ * sorted by cost (largest first).
+ */
+dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_steps,
+                        const float* coeffs, int32_t n_coeff_triples, float eps,
+                        dmuon_dtypes dtypes, uint32_t flags, dmuon_plan_t* out);
+
+/* Bytes of device workspace the plan needs (host only). */
+dmuon_status dmuon_plan_workspace_bytes(dmuon_plan_t plan, size_t* bytes);
+
+/*
+ * dmuon_plan_bind - attach a caller-owned device workspace and upload the
+ * plan's tables into it (asynchronously, on stream).
+ *
+ *  d_workspace  device pointer, 1024-byte aligned, at least
+ *               dmuon_plan_workspace_bytes() bytes; owned by the caller and
+ *               used exclusively by this plan until it is destroyed or bound
+ *               again. Its contents need not be initialised.
+ *  Builds the TMA tensor maps for the workspace buffers. The plan's host
+ *  staging of the tables must outlive the copies: it does (it is owned by the
+ *  plan). Returns DMUON_ERR_WORKSPACE if the buffer is NULL, misaligned or
+ *  too small.
+ */
+dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes, void* stream);
+
+/*
+ * dmuon_step - one Muon step for every matrix of the plan, asynchronous on
+ * stream.
+ *
+ *  params[n_mats]   host array of device pointers; W_i, rows x cols,
+ *                   param dtype, updated in place.
+ *  grads[n_mats]    host array of device pointers; G_i, grad dtype, read only.
+ *  momenta[n_mats]  host array of device pointers; M_i, fp32, updated in place.
+ *  lr, mu           learning rate and momentum coefficient (finite).
+ *  nesterov         0 = heavy ball (U = M), 1 = Nesterov (U = G + mu*M).
+ *
+ * Each pointer must be 16-byte aligned and the matrices must not overlap.
+ * The host pointer arrays are read during the call only. When the set of
+ * pointers differs from the previous call's it is uploaded with a
+ * cudaMemcpyAsync from host memory; under CUDA-graph capture, make one
+ * uncaptured call with the same pointers first so that none is needed.
+ * Launches 1 + 3*ns_steps kernels (1 + 1 when ns_steps == 0; more when the
+ * plan has more than 8 buckets).
+ */
+dmuon_status dmuon_step(dmuon_plan_t plan, void* const* params, const void* const* grads,
+                        void* const* momenta, float lr, float mu, int32_t nesterov, void* stream);
+
+/*
+ * dmuon_read_device_status - synchronise stream, return the device status
+ * bits accumulated since the last read (DMUON_DEV_*) in *bits, and clear
+ * them. Returns DMUON_OK even when bits are set.
+ */
+dmuon_status dmuon_read_device_status(dmuon_plan_t plan, void* stream, uint32_t* bits);
+
+/*
+ * dmuon_read_update - copy the fp32 update X of matrix `mat` from the last
+ * step (before lr and the shape scale, in W's rows x cols orientation) to
+ * d_dst (device, rows*cols floats), asynchronously on stream. Needs a plan
+ * made with DMUON_FLAG_CAPTURE_UPDATE.
+ */
+dmuon_status dmuon_read_update(dmuon_plan_t plan, int32_t mat, float* d_dst, void* stream);
+
+/*
+ * dmuon_plan_describe - JSON text describing the plan (buckets, tiles per
+ * phase, launches per step, algorithmic flops and bytes per launch) written
+ * to buf (at most len bytes, NUL-terminated); *needed receives the full
+ * length + 1. Host only.
+ */
+dmuon_status dmuon_plan_describe(dmuon_plan_t plan, char* buf, size_t len, size_t* needed);
+
+/*
+ * Profiling: dmuon_profile_begin(plan, max_launches) makes the following
+ * steps record a CUDA event pair around each launch (on the step's stream),
+ * for up to max_launches launches (it creates the events: host-side CUDA
+ * objects, no device memory). dmuon_profile_end synchronises the events and
+ * writes, for each recorded launch i < cap, its kind (DMUON_KIND_*), its
+ * duration in ms and its algorithmic work (flops for GEMM kinds, bytes for
+ * streaming kinds); *n receives the number recorded. Profiling then stops.
+ */
+dmuon_status dmuon_profile_begin(dmuon_plan_t plan, int32_t max_launches);
+dmuon_status dmuon_profile_end(dmuon_plan_t plan, int32_t* kinds, float* ms, double* work,
+                               int32_t cap, int32_t* n);
+
+/* Number of kernels the library has launched through this plan so far. */
+dmuon_status dmuon_launch_count(dmuon_plan_t plan, int64_t* count);
+
+/*
+ * dmuon_selftest_wait_timeout - run one small kernel whose pipeline wait can
+ * never complete (nothing arrives on its barrier), with a wait limit of
+ * limit_ns nanoseconds (1e6..5e9). The kernel gives up, records
+ * DMUON_DEV_WAIT_TIMEOUT and returns; *bits receives the status it wrote.
+ * Exercises the bounded-wait path of the pipelined kernels without a fault.
+ * Synchronises stream. d_scratch: 256 device bytes owned by the caller.
+ */
+dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void* stream,
+                                         uint32_t* bits);
+
+/* Free the host-side plan (the workspace stays the caller's). NULL is a no-op. */
+void dmuon_plan_destroy(dmuon_plan_t plan);
+
+/* Message of the last error on this thread ("" if none). */
+const char* dmuon_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t dmuon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMUON_H */

@@ -1,0 +1,134 @@
+// internal.h - structures shared by the host planner and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dmuon.h"
+
+namespace dmuon {
+
+constexpr int kMaxBucketsPerLaunch = 8;
+
+// Tensor-core tile: 128 rows (UMMA M) x 256 columns (UMMA N), K staged 64 at a time.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 64;
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+
+// fp32 SIMT tile.
+constexpr int kSimtBM = 64;
+constexpr int kSimtBN = 64;
+constexpr int kSimtBK = 16;
+constexpr int kSimtThreads = 256;
+
+// Streaming unit of the momentum pass: 8192 contiguous elements (flat mode)
+// or a 64 x 128 tile of the stored matrix (tiled mode).
+constexpr int kFlatUnit = 8192;
+constexpr int kTileR = 64;
+constexpr int kTileC = 128;
+constexpr int kStreamThreads = 256;
+
+enum Phase : int { kPhaseGram = 1, kPhasePoly = 2, kPhaseGemm = 3 };
+
+// Per-matrix description (device table, uploaded once at bind).
+struct MatDev {
+  int32_t rows, cols;   // stored shape (rows = dim 0)
+  int32_t m, n;         // short and long side
+  int32_t transposed;   // rows > cols: the iteration runs on the transpose
+  int32_t bucket, slot; // bucket index and position inside it
+  int32_t x_ld;         // row pitch (elements) of the U/X copies in the workspace
+  float scale;          // sqrt(max(1, rows/cols))
+  int32_t flat;         // momentum pass mode: 1 = flat contiguous, 0 = 64x128 tiles
+  int32_t tiles_c;      // tiled mode: tiles along cols
+  int32_t vec_ok;       // tiled mode: cols % 4 == 0 (vector loads allowed)
+  int64_t x0_off;       // byte offset from the workspace base of this matrix's X0 (= U)
+  int64_t unit_begin;   // first momentum-pass unit of this matrix
+  int64_t unit_count;
+  int64_t cap_off;      // element offset in the capture buffer, -1 when not captured
+};
+
+// Momentum / normalisation pass.
+struct StreamParams {
+  const MatDev* mats;
+  const int64_t* unit_begin;  // [n_mats + 1]
+  const uint64_t* ptrs;       // [3 * n_mats]: W, G, M device pointers
+  char* ws;
+  float* partial;             // [n_units]
+  unsigned* counters;         // [n_mats], zero between launches
+  float* s_norm;              // [n_mats]: 1 / (||U||_F + eps)
+  unsigned* status;
+  float* capture;
+  int64_t n_units;
+  int32_t n_mats;
+  float mu, eps, lr;
+  int32_t nesterov;
+  int32_t grad_bf16, x_bf16, param_bf16;
+};
+
+// One bucket as seen by a tensor-core launch.
+struct TcBucket {
+  CUtensorMap tmA;  // A operand: 128 x 64 boxes, K-major
+  CUtensorMap tmB;  // B operand: 256 x 64 boxes K-major (gram/poly) or 64 x 64 boxes MN-major (gemm)
+  const int32_t* slot_mat;  // slot -> global matrix index
+  char* out;                // A (gram), B (poly), X_{k+1} (gemm, not last)
+  const char* aux;          // A (poly: b*A term), X_k (gemm: a*X term)
+  int64_t out_mat_stride;   // bytes between consecutive matrices of out
+  int64_t aux_mat_stride;
+  int32_t out_ld, aux_ld;   // row pitch in elements
+  int32_t m, n, kdim;
+  int32_t pad;
+};
+
+struct TcParams {
+  TcBucket bk[kMaxBucketsPerLaunch];
+  const int4* items;  // (bucket, slot, ti, tj), cost-ordered
+  int32_t n_items;
+  int32_t first, last;
+  float a, b, c, lr;
+  const MatDev* mats;
+  const uint64_t* ptrs;
+  const float* s_norm;
+  float* capture;
+  unsigned* status;
+  int32_t param_bf16;
+  int64_t timeout_ns;
+};
+
+// One bucket as seen by a fp32 SIMT launch.
+struct SimtBucket {
+  const int32_t* slot_mat;
+  const float* opA;   // gram: X (m x n); poly: A (m x m); gemm: B (m x m)
+  const float* opB;   // gram: X; poly: A; gemm: X_k
+  float* out;
+  const float* aux;
+  int64_t a_mat_stride, b_mat_stride, out_mat_stride, aux_mat_stride;  // elements
+  int32_t a_ld, b_ld, out_ld, aux_ld;
+  int32_t m, n, kdim, pad;
+};
+
+struct SimtParams {
+  SimtBucket bk[kMaxBucketsPerLaunch];
+  const int4* items;
+  int32_t n_items;
+  int32_t first, last;
+  float a, b, c, lr;
+  const MatDev* mats;
+  const uint64_t* ptrs;
+  const float* s_norm;
+  float* capture;
+  int32_t param_bf16;
+};
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s);
+cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s);
+cudaError_t launch_tc(int phase, const TcParams& p, int grid, cudaStream_t s);
+cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
+size_t tc_smem_bytes();
+
+}  // namespace dmuon

@@ -1,0 +1,332 @@
+// momentum.cu - the streaming pass in front of Newton-Schulz.
+//
+// One launch over every matrix of the batch:
+//   M <- mu*M + G;  U = G + mu*M (Nesterov) or U = M      (fp32 math, M in place)
+//   U is written to the matrix's workspace slot in the compute dtype, already
+//   in the short-side orientation (transposed through shared memory when
+//   rows > cols), and sum(U^2) is reduced per matrix, deterministically:
+//   each work unit writes one fp32 partial, and the CTA that finishes a
+//   matrix's last unit (an atomic ticket, no waiting) adds that matrix's
+//   partials in a fixed order in fp64 and stores s = 1 / (sqrt(sum) + eps).
+// The Newton-Schulz kernels fold s into their first-step epilogues, so U is
+// never rescaled in HBM. ("momentum-aggregated gradients", "DMuon: Efficient
+// Distributed Muon Training with Near-Adam Overhead", gist.science summary
+// section 1.)
+//
+// HBM-bound: per element it reads G (2 or 4 B) and M (4 B) and writes M (4 B)
+// and U (2 or 4 B). Work units: 8192 contiguous elements when the stored
+// matrix and its slot share a layout (rows <= cols, cols % 8 == 0), else
+// 64 x 128 tiles of the stored matrix.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace dmuon {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ int find_matrix(const int64_t* unit_begin, int n_mats, int64_t u) {
+  int lo = 0, hi = n_mats;  // unit_begin[lo] <= u < unit_begin[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (unit_begin[mid] <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+template <bool GB>
+__device__ __forceinline__ void load8_grad(const void* g, int64_t e, float (&x)[8]) {
+  if (GB) {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(g) + e);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e);
+    const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e + 4);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+  }
+}
+
+template <bool XB>
+__device__ __forceinline__ void store8_x(void* dst, int64_t e, const float (&u)[8]) {
+  if (XB) {
+    uint4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(dst) + e) = o;
+  } else {
+    float* d = reinterpret_cast<float*>(dst) + e;
+    *reinterpret_cast<float4*>(d) = make_float4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<float4*>(d + 4) = make_float4(u[4], u[5], u[6], u[7]);
+  }
+}
+
+template <bool GB>
+__device__ __forceinline__ float load1_grad(const void* g, int64_t e) {
+  return GB ? __bfloat162float(reinterpret_cast<const bf16*>(g)[e]) : reinterpret_cast<const float*>(g)[e];
+}
+
+template <bool XB>
+__device__ __forceinline__ void store1_x(void* dst, int64_t e, float v) {
+  if (XB)
+    reinterpret_cast<bf16*>(dst)[e] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(dst)[e] = v;
+}
+
+__device__ __forceinline__ float block_sum_f(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x == 0)
+    for (int k = 0; k < kStreamThreads / 32; ++k) t += red[k];
+  return t;  // valid in thread 0
+}
+
+__device__ __forceinline__ double block_sum_d(double v, double* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0)
+    for (int k = 0; k < kStreamThreads / 32; ++k) t += red[k];
+  return t;
+}
+
+template <bool GB, bool XB>
+__global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_constant__ StreamParams p) {
+  __shared__ float tileU[kTileR][kTileC + 1];
+  __shared__ float redf[kStreamThreads / 32];
+  __shared__ double redd[kStreamThreads / 32];
+  __shared__ int is_last;
+  const float mu = p.mu;
+  const bool nest = p.nesterov != 0;
+
+  for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const int mat = find_matrix(p.unit_begin, p.n_mats, u);
+    const MatDev md = p.mats[mat];
+    const int64_t local = u - md.unit_begin;
+    const void* G = reinterpret_cast<const void*>(p.ptrs[p.n_mats + mat]);
+    float* M = reinterpret_cast<float*>(p.ptrs[2 * p.n_mats + mat]);
+    void* X = p.ws + md.x0_off;
+    float ss = 0.f;
+
+    if (md.flat) {
+      const int64_t total = (int64_t)md.rows * md.cols;
+      const int64_t e0 = local * kFlatUnit;
+      const int64_t e1 = min(e0 + kFlatUnit, total);
+#pragma unroll
+      for (int k = 0; k < kFlatUnit / (8 * kStreamThreads); ++k) {
+        const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
+        if (e + 8 <= e1) {
+          float g[8], uu[8];
+          load8_grad<GB>(G, e, g);
+          float4 m0 = *reinterpret_cast<const float4*>(M + e);
+          float4 m1 = *reinterpret_cast<const float4*>(M + e + 4);
+          float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            mv[q] = fmaf(mu, mv[q], g[q]);
+            uu[q] = nest ? fmaf(mu, mv[q], g[q]) : mv[q];
+            ss = fmaf(uu[q], uu[q], ss);
+          }
+          *reinterpret_cast<float4*>(M + e) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+          *reinterpret_cast<float4*>(M + e + 4) = make_float4(mv[4], mv[5], mv[6], mv[7]);
+          store8_x<XB>(X, e, uu);
+        } else {
+          for (int64_t q = e; q < e1 && q < e + 8; ++q) {
+            const float g = load1_grad<GB>(G, q);
+            const float mv = fmaf(mu, M[q], g);
+            const float uu = nest ? fmaf(mu, mv, g) : mv;
+            M[q] = mv;
+            store1_x<XB>(X, q, uu);
+            ss = fmaf(uu, uu, ss);
+          }
+        }
+      }
+    } else {
+      const int tr = static_cast<int>(local / md.tiles_c), tc = static_cast<int>(local % md.tiles_c);
+      const int r0 = tr * kTileR, c0 = tc * kTileC;
+      // read 64 x 128 of G and M (4 consecutive columns per thread), update M, keep U in smem
+#pragma unroll 2
+      for (int pass = 0; pass < kTileR / 8; ++pass) {
+        const int rr = pass * 8 + (threadIdx.x >> 5);
+        const int cc = (threadIdx.x & 31) * 4;
+        const int r = r0 + rr, c = c0 + cc;
+        float uu[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < md.rows) {
+          const int64_t e = (int64_t)r * md.cols + c;
+          if (md.vec_ok && c + 4 <= md.cols) {
+            float g[4];
+            if (GB) {
+              const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e);
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+              const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
+              g[0] = f0.x, g[1] = f0.y, g[2] = f1.x, g[3] = f1.y;
+            } else {
+              const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e);
+              g[0] = f.x, g[1] = f.y, g[2] = f.z, g[3] = f.w;
+            }
+            const float4 m4 = *reinterpret_cast<const float4*>(M + e);
+            float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              mv[q] = fmaf(mu, mv[q], g[q]);
+              uu[q] = nest ? fmaf(mu, mv[q], g[q]) : mv[q];
+              ss = fmaf(uu[q], uu[q], ss);
+            }
+            *reinterpret_cast<float4*>(M + e) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+          } else {
+            for (int q = 0; q < 4 && c + q < md.cols; ++q) {
+              const float g = load1_grad<GB>(G, e + q);
+              const float mv = fmaf(mu, M[e + q], g);
+              M[e + q] = mv;
+              uu[q] = nest ? fmaf(mu, mv, g) : mv;
+              ss = fmaf(uu[q], uu[q], ss);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tileU[rr][cc + q] = uu[q];
+      }
+      __syncthreads();
+      if (md.transposed) {
+        // U^T rows: slot element (c, r) at c*x_ld + r; 8 consecutive r per thread
+#pragma unroll
+        for (int pass = 0; pass < kTileC / 32; ++pass) {
+          const int jj = pass * 32 + (threadIdx.x >> 3);
+          const int ii = (threadIdx.x & 7) * 8;
+          const int c = c0 + jj, r = r0 + ii;
+          if (c >= md.cols) continue;
+          const int64_t e = (int64_t)c * md.x_ld + r;
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = tileU[ii + q][jj];
+          if (r + 8 <= md.rows) {
+            store8_x<XB>(X, e, v);
+          } else {
+            for (int q = 0; q < 8 && r + q < md.rows; ++q) store1_x<XB>(X, e + q, v[q]);
+          }
+        }
+      } else {
+        // same orientation, row pitch x_ld
+#pragma unroll 2
+        for (int pass = 0; pass < kTileR / 8; ++pass) {
+          const int rr = pass * 8 + (threadIdx.x >> 5);
+          const int cc = (threadIdx.x & 31) * 4;
+          const int r = r0 + rr, c = c0 + cc;
+          if (r >= md.rows) continue;
+          const int64_t e = (int64_t)r * md.x_ld + c;
+          for (int q = 0; q < 4 && c + q < md.cols; ++q) store1_x<XB>(X, e + q, tileU[rr][cc + q]);
+        }
+      }
+    }
+
+    // per-unit partial, then the last unit of the matrix finalises s
+    const float bs = block_sum_f(ss, redf);
+    if (threadIdx.x == 0) {
+      p.partial[u] = bs;
+      __threadfence();
+      const unsigned t = atomicAdd(&p.counters[mat], 1u);
+      is_last = (t == static_cast<unsigned>(md.unit_count - 1));
+    }
+    __syncthreads();
+    if (is_last) {
+      __threadfence();
+      double acc = 0.0;
+      for (int64_t k = threadIdx.x; k < md.unit_count; k += kStreamThreads)
+        acc += static_cast<double>(__ldcg(&p.partial[md.unit_begin + k]));
+      const double tot = block_sum_d(acc, redd);
+      if (threadIdx.x == 0) {
+        const float nrm = static_cast<float>(sqrt(tot));
+        if (!isfinite(nrm)) atomicOr(p.status, DMUON_DEV_NONFINITE_NORM);
+        p.s_norm[mat] = 1.0f / (nrm + p.eps);
+        p.counters[mat] = 0u;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ns_steps == 0: W -= lr * scale * s * U (U read back from the slot).
+template <bool XB>
+__global__ void __launch_bounds__(kStreamThreads) update0_kernel(const __grid_constant__ StreamParams p) {
+  for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    const int mat = find_matrix(p.unit_begin, p.n_mats, u);
+    const MatDev md = p.mats[mat];
+    const int64_t local = u - md.unit_begin;
+    const float f = p.lr * md.scale * p.s_norm[mat];
+    const char* X = p.ws + md.x0_off;
+    void* W = reinterpret_cast<void*>(p.ptrs[mat]);
+    int64_t e0, e1;
+    int r0 = 0, c0 = 0;
+    if (md.flat) {
+      e0 = local * kFlatUnit;
+      e1 = min(e0 + kFlatUnit, (int64_t)md.rows * md.cols);
+    } else {
+      r0 = static_cast<int>(local / md.tiles_c) * kTileR;
+      c0 = static_cast<int>(local % md.tiles_c) * kTileC;
+      e0 = 0;
+      e1 = kTileR * kTileC;
+    }
+    for (int64_t q = e0 + threadIdx.x; q < e1; q += kStreamThreads) {
+      int64_t widx, xidx;
+      if (md.flat) {
+        widx = xidx = q;
+      } else {
+        const int r = r0 + static_cast<int>(q / kTileC), c = c0 + static_cast<int>(q % kTileC);
+        if (r >= md.rows || c >= md.cols) continue;
+        widx = (int64_t)r * md.cols + c;
+        xidx = md.transposed ? (int64_t)c * md.x_ld + r : (int64_t)r * md.x_ld + c;
+      }
+      const float x = XB ? __bfloat162float(reinterpret_cast<const bf16*>(X)[xidx])
+                         : reinterpret_cast<const float*>(X)[xidx];
+      if (p.param_bf16) {
+        bf16* w = reinterpret_cast<bf16*>(W);
+        w[widx] = __float2bfloat16_rn(__bfloat162float(w[widx]) - f * x);
+      } else {
+        reinterpret_cast<float*>(W)[widx] -= f * x;
+      }
+      if (p.capture != nullptr && md.cap_off >= 0) p.capture[md.cap_off + widx] = p.s_norm[mat] * x;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s) {
+  if (p.grad_bf16 && p.x_bf16)
+    momentum_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(p);
+  else if (p.grad_bf16)
+    momentum_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(p);
+  else if (p.x_bf16)
+    momentum_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
+  else
+    momentum_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s) {
+  if (p.x_bf16)
+    update0_kernel<true><<<grid, kStreamThreads, 0, s>>>(p);
+  else
+    update0_kernel<false><<<grid, kStreamThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dmuon

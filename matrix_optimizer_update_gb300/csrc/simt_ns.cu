@@ -1,0 +1,139 @@
+// simt_ns.cu - fp32 arithmetic mode of the Newton-Schulz products.
+//
+// Same three phases as the tensor-core path (gram A = X X^T on upper tiles
+// with mirrored stores; poly B = b*A + c*A A^T; gemm X' = a*X + B X with the
+// W update fused into the last step), computed with fp32 FFMA on CUDA cores:
+// TF32 tensor math keeps only 10 mantissa bits and cannot reach fp32-level
+// agreement. One 64 x 64 output tile per CTA, 256 threads, 4 x 4 outputs per
+// thread, K staged 16 at a time through shared memory.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace dmuon {
+namespace {
+
+template <int PHASE>
+__global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_constant__ SimtParams p) {
+  __shared__ float As[kSimtBK][kSimtBM + 4];  // As[k][row]
+  __shared__ float Bs[kSimtBK][kSimtBN + 4];  // Bs[k][col]
+  const int4 it = p.items[blockIdx.x];
+  const SimtBucket& B = p.bk[it.x];
+  const int slot = it.y;
+  const int row0 = it.z * kSimtBM, col0 = it.w * kSimtBN;
+  const float* opA = B.opA + slot * B.a_mat_stride;
+  const float* opB = B.opB + slot * B.b_mat_stride;
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int m = B.m, kdim = B.kdim;
+  // output columns are bounded by m (gram/poly) or n (gemm)
+  const int ncols = (PHASE == kPhaseGemm) ? B.n : B.m;
+
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+
+  for (int k0 = 0; k0 < kdim; k0 += kSimtBK) {
+    // A operand rows row0.., K contiguous in memory
+    for (int e = tid; e < kSimtBM * kSimtBK; e += kSimtThreads) {
+      const int r = e / kSimtBK, k = e % kSimtBK;
+      const int gr = row0 + r, gk = k0 + k;
+      As[k][r] = (gr < m && gk < kdim) ? opA[(int64_t)gr * B.a_ld + gk] : 0.f;
+    }
+    if (PHASE == kPhaseGemm) {
+      // B operand = X_k rows k (K), columns col0.. contiguous in memory
+      for (int e = tid; e < kSimtBN * kSimtBK; e += kSimtThreads) {
+        const int k = e / kSimtBN, c = e % kSimtBN;
+        const int gk = k0 + k, gc = col0 + c;
+        Bs[k][c] = (gk < kdim && gc < ncols) ? opB[(int64_t)gk * B.b_ld + gc] : 0.f;
+      }
+    } else {
+      // B operand = rows col0.. of the same matrix (the product with its transpose)
+      for (int e = tid; e < kSimtBN * kSimtBK; e += kSimtThreads) {
+        const int c = e / kSimtBK, k = e % kSimtBK;
+        const int gc = col0 + c, gk = k0 + k;
+        Bs[k][c] = (gc < ncols && gk < kdim) ? opB[(int64_t)gc * B.b_ld + gk] : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kSimtBK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = As[k][ty * 4 + r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) b[c] = Bs[k][tx * 4 + c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+
+  const int gm = B.slot_mat[slot];
+  const MatDev md = p.mats[gm];
+  float sc = 1.f;
+  if (p.first) {
+    const float s = p.s_norm[gm];
+    sc = (PHASE == kPhaseGram) ? s * s : (PHASE == kPhaseGemm ? s : 1.f);
+  }
+  float* out = B.out ? B.out + slot * B.out_mat_stride : nullptr;
+  const float* aux = B.aux ? B.aux + slot * B.aux_mat_stride : nullptr;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = row0 + ty * 4 + r;
+    if (i >= m) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = col0 + tx * 4 + c;
+      if (j >= ncols) continue;
+      float v = acc[r][c];
+      if (PHASE == kPhaseGram || PHASE == kPhasePoly) {
+        if (j < i) continue;
+        v = (PHASE == kPhaseGram) ? v * sc : p.b * aux[(int64_t)i * B.aux_ld + j] + p.c * v;
+        out[(int64_t)i * B.out_ld + j] = v;
+        out[(int64_t)j * B.out_ld + i] = v;
+      } else {
+        v = (p.a * aux[(int64_t)i * B.aux_ld + j] + v) * sc;
+        if (!p.last) {
+          out[(int64_t)i * B.out_ld + j] = v;
+          continue;
+        }
+        const float step = p.lr * md.scale;
+        const int64_t widx = md.transposed ? (int64_t)j * m + i : (int64_t)i * B.n + j;
+        if (p.param_bf16) {
+          __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(p.ptrs[gm]);
+          w[widx] = __float2bfloat16_rn(__bfloat162float(w[widx]) - step * v);
+        } else {
+          float* w = reinterpret_cast<float*>(p.ptrs[gm]);
+          w[widx] -= step * v;
+        }
+        if (p.capture != nullptr && md.cap_off >= 0) p.capture[md.cap_off + widx] = v;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s) {
+  switch (phase) {
+    case kPhaseGram:
+      simt_ns_kernel<kPhaseGram><<<grid, kSimtThreads, 0, s>>>(p);
+      break;
+    case kPhasePoly:
+      simt_ns_kernel<kPhasePoly><<<grid, kSimtThreads, 0, s>>>(p);
+      break;
+    case kPhaseGemm:
+      simt_ns_kernel<kPhaseGemm><<<grid, kSimtThreads, 0, s>>>(p);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dmuon

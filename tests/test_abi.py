@@ -1,0 +1,135 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/dmuon.h declares, and the host planner validates, buckets and
+counts tiles as stated."""
+
+import os
+import re
+
+import pytest
+
+from matrix_optimizer_update_gb300 import dmuon as dm
+from matrix_optimizer_update_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dmuon.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dmuon_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(dm.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = dm.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert dm.dmuon_version() >= 100
+
+
+def test_invalid_arguments_are_rejected_on_the_host():
+    with pytest.raises(dm.DmuonError) as e:
+        dm.dmuon_plan([], 5)
+    assert e.value.status == dm.ERR_INVALID_ARG
+    for bad in ([(0, 4)], [(4, -1)], [(1 << 21, 4)], [(65536, 65536)]):
+        with pytest.raises(dm.DmuonError) as e:
+            dm.dmuon_plan(bad, 5)
+        assert e.value.status == dm.ERR_INVALID_ARG
+    with pytest.raises(dm.DmuonError) as e:
+        dm.dmuon_plan([(4, 4)], 17)
+    assert e.value.status == dm.ERR_INVALID_ARG
+    with pytest.raises(dm.DmuonError) as e:
+        dm.dmuon_plan([(4, 4)], 3, coeffs=[(1, 2, 3), (1, 2, 3)])
+    assert e.value.status == dm.ERR_INVALID_ARG
+    with pytest.raises(dm.DmuonError) as e:
+        dm.dmuon_plan([(4, 4)], 3, eps=-1.0)
+    assert e.value.status == dm.ERR_INVALID_ARG
+    with pytest.raises(dm.DmuonError) as e:
+        dm.dmuon_plan([(4, 4)], 3, flags=0x80)
+    assert e.value.status == dm.ERR_UNSUPPORTED
+
+
+def test_step_before_bind_is_refused():
+    p = dm.dmuon_plan([(8, 16)], 5)
+    with pytest.raises(dm.DmuonError) as e:
+        p.step([16], [32], [48], 0.02, 0.95, True, 0)
+    assert e.value.status == dm.ERR_NOT_BOUND
+    with pytest.raises(dm.DmuonError) as e:
+        p.bind(0, 1 << 20, 0)
+    assert e.value.status == dm.ERR_WORKSPACE
+    with pytest.raises(dm.DmuonError) as e:
+        p.bind(1024 * 7 + 16, 1 << 40, 0)  # misaligned
+    assert e.value.status == dm.ERR_WORKSPACE
+    with pytest.raises(dm.DmuonError) as e:
+        p.bind(1024 * 1024, 16, 0)  # too small
+    assert e.value.status == dm.ERR_WORKSPACE
+    with pytest.raises(dm.DmuonError) as e:
+        p.read_update(0, 1024, 0)
+    assert e.value.status == dm.ERR_UNSUPPORTED
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def brute_tiles(m, n, bm, bn):
+    gram = sum(1 for ti in range(cdiv(m, bm)) for tj in range(cdiv(m, bn)) if tj * bn + bn - 1 >= ti * bm)
+    gemm = cdiv(m, bm) * cdiv(n, bn)
+    return gram, gemm
+
+
+@pytest.mark.parametrize("name", ["toy", "qwen2.5-1.5b", "llama-3.2-3b", "llama-3.1-8b", "moe-16x64"])
+def test_plan_buckets_tiles_and_work(name):
+    w = wl.get(name)
+    p = dm.dmuon_plan(w.shapes, w.ns_steps, w.coeffs, w.eps, w.param_dtype, w.grad_dtype, w.compute)
+    d = p.describe()
+    bm, bn = d["tile"]
+    # buckets: one per distinct (short, long) shape, counts and transposed counts add up
+    want = {}
+    for r, c in w.shapes:
+        k = (min(r, c), max(r, c))
+        cnt, tr = want.get(k, (0, 0))
+        want[k] = (cnt + 1, tr + (r > c))
+    got = {(b["m"], b["n"]): (b["count"], b["transposed"]) for b in d["buckets"]}
+    assert got == want
+    # tile counts: upper-triangle tiles for the symmetric products, full grid for the gemm
+    g_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, bn)[0] for b in d["buckets"])
+    m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, bn)[1] for b in d["buckets"])
+    assert sum(c["gram"] for c in d["lists"]) == g_tot
+    assert sum(c["poly"] for c in d["lists"]) == g_tot
+    assert sum(c["gemm"] for c in d["lists"]) == m_tot
+    # launches per step and the algorithmic work the profiler attributes to them
+    assert len(d["launches"]) == 1 + 3 * w.ns_steps * d["chunks"]
+    work = {}
+    for L in d["launches"]:
+        work[L["kind"]] = work.get(L["kind"], 0.0) + L["work"]
+    flops = sum(wl.ns_flops(r, c, w.ns_steps) for r, c in w.shapes)
+    assert abs(work[dm.KIND_GRAM] + work[dm.KIND_POLY] + work[dm.KIND_GEMM] - flops) / flops < 1e-12
+    xel = 2 if w.compute == "bf16" else 4
+    gb = 2 if w.grad_dtype == "bf16" else 4
+    assert work[dm.KIND_MOMENTUM] == sum(r * c for r, c in w.shapes) * (gb + 8 + xel)
+    assert p.workspace_bytes() > 0
+
+
+def test_many_buckets_split_into_chunks():
+    shapes = [(16 * (k + 1), 256) for k in range(19)]
+    p = dm.dmuon_plan(shapes, 2)
+    d = p.describe()
+    assert d["chunks"] == 3 and len(d["buckets"]) == 19
+    assert len(d["launches"]) == 1 + 3 * 2 * 3
+
+
+def test_ns_steps_zero_plan():
+    p = dm.dmuon_plan([(64, 128), (128, 64)], 0)
+    kinds = [L["kind"] for L in p.describe()["launches"]]
+    assert kinds == [dm.KIND_MOMENTUM, dm.KIND_UPDATE0]
+
+
+def test_plan_is_deterministic():
+    w = wl.get("moe-16x64")
+    a = dm.dmuon_plan(w.shapes, 5).describe()
+    b = dm.dmuon_plan(w.shapes, 5).describe()
+    assert a == b
