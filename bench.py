@@ -57,6 +57,18 @@ def aggregate(flops_per_step_per_rank: float, steps: int, world: int, max_second
     return flops_per_step_per_rank * steps * world / max_seconds / 1e12
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -222,6 +234,10 @@ def run_ours(args):
     torch.cuda.set_device(local)
     build_mod.build()
     w = wl.get(args.workload)
+    if args.layers:
+        import dataclasses
+
+        w = dataclasses.replace(w, layers=args.layers, name=f"{w.name}[{args.layers} layers]")
     tot = wl.totals(w)
     ms = make_matrix_set(w, f"cuda:{local}", seed_offset=replica_seed_offset(rank))
     stream = torch.cuda.Stream()
@@ -268,13 +284,7 @@ def run_ours(args):
     clk = clocks.stop()
     status = plan.read_device_status(sh)
 
-    max_ms = elapsed_ms
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([elapsed_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(elapsed_ms, world, f"cuda:{local}")
 
     # ---- per-kind accounting from the live events
     per_kind = {}
@@ -331,13 +341,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([e2e_ms], device=f"cuda:{local}")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, f"cuda:{local}")
         e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
                "h2d_bytes_per_step": hG.numel() * hG.element_size(),
@@ -383,6 +387,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama-3.1-8b")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0, help="truncate the workload to its first N layers (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
