@@ -209,6 +209,37 @@ dmuon_status dmuon_launch_count(dmuon_plan_t plan, int64_t* count);
 dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void* stream,
                                          uint32_t* bits);
 
+/*
+ * dmuon_momentum_norm_noalloc - the momentum and normalisation pass of ONE
+ * matrix for callers that cannot allocate device memory: a framework whose
+ * allocator already holds the whole GPU, a plugin handed only the tensors it
+ * must update, or a runtime that forbids allocation in its steady state.
+ * The pages have no counterpart; it is the plan-free form of the first
+ * launch of dmuon_step, with its reduction scratch (per-tile partial sums
+ * and a ticket counter) in a static device array of the library instead of
+ * a workspace.
+ *
+ *  grad       device, rows x cols, grad_dtype (DMUON_F32 or DMUON_BF16), read only.
+ *  momentum   device, rows x cols fp32, updated in place: M <- mu*M + G.
+ *  u_out      device, m x u_ld elements of u_dtype, m = min(rows, cols),
+ *             u_ld = round_up(max(rows, cols), 8): U = G + mu*M (Nesterov) or
+ *             U = M, stored transposed when rows > cols (short side first).
+ *  s_out      device, one float: 1 / (||U||_F + eps).
+ *
+ * Limit: ceil(rows/64) * ceil(cols/128) <= 65536 (e.g. 8192 x 8192 fits);
+ * larger matrices return DMUON_ERR_UNSUPPORTED. The static array (256 KiB +
+ * 256 B) stays allocated on every GPU that loads the library until the
+ * process exits. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. The call allocates nothing: it issues one
+ * cudaMemsetAsync (clearing the ticket counter) and one kernel on stream.
+ * Every call shares the array and it keeps the last call's contents; calls
+ * that overlap on the GPU race and give wrong results.
+ */
+dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* momentum, void* u_out, float* s_out,
+                                         int64_t rows, int64_t cols, int32_t grad_dtype, int32_t u_dtype,
+                                         float mu, int32_t nesterov, float eps, void* stream);
+
 /* Free the host-side plan (the workspace stays the caller's). NULL is a no-op. */
 void dmuon_plan_destroy(dmuon_plan_t plan);
 

@@ -379,6 +379,11 @@ void destroy_events(dmuon_plan_s& P) {
 
 }  // namespace
 
+dmuon_status dmuon::set_last_error(dmuon_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+
 // ============================================================================ C ABI
 extern "C" {
 

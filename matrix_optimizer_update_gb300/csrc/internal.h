@@ -131,4 +131,7 @@ cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s
 cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
 size_t tc_smem_bytes();
 
+// Record the message dmuon_last_error() returns on this thread; returns st.
+dmuon_status set_last_error(dmuon_status st, const char* msg);
+
 }  // namespace dmuon

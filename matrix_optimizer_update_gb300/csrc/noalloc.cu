@@ -1,0 +1,208 @@
+// noalloc.cu - the momentum / normalisation pass for ONE matrix without any
+// caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// optimizer: a framework whose caching allocator has already reserved the
+// whole GPU, a plugin that is handed only the tensors it must update, or a
+// runtime that forbids allocation once its steady state has begun. The
+// regular pass (momentum.cu) keeps its per-unit partial sums and per-matrix
+// tickets in the caller's workspace; this variant keeps them in a file-scope
+// static device array instead, so the caller passes only inputs and outputs.
+//
+// The array lives in every GPU that loads the library until the process
+// exits; it holds kNoallocMaxUnits fp32 partial sums plus one ticket counter
+// (256 KiB + 256 B). All calls share it: calls that overlap on the GPU (two
+// streams, or two host threads) race on it and give wrong results.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "dmuon.h"
+#include "internal.h"
+
+namespace dmuon {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kNoallocMaxUnits = 65536;  // 64 x 128 tiles per matrix
+constexpr int kNoallocCounterSlot = kNoallocMaxUnits;  // the ticket counter sits after the partials
+constexpr int kNoallocWords = kNoallocMaxUnits + 64;
+
+// Static scratch: [0, kNoallocMaxUnits) fp32 partial sums (as raw words), then the ticket counter.
+static __device__ __align__(256) unsigned g_noalloc_scratch[kNoallocWords];
+
+struct NoallocParams {
+  const void* grad;
+  float* momentum;
+  void* u;
+  float* s_out;
+  unsigned* scratch;  // device address of g_noalloc_scratch
+  int32_t rows, cols, u_ld, tiles_c;
+  int32_t n_tiles;
+  int32_t transposed;
+  float mu, eps;
+  int32_t nesterov;
+};
+
+template <bool GB, bool XB>
+__global__ void __launch_bounds__(kStreamThreads) momentum_norm_noalloc_kernel(const __grid_constant__ NoallocParams p) {
+  __shared__ float tileU[kTileR][kTileC + 1];
+  __shared__ float red[kStreamThreads / 32];
+  __shared__ double redd[kStreamThreads / 32];
+  __shared__ int is_last;
+  float* partial = reinterpret_cast<float*>(p.scratch);
+  unsigned* counter = p.scratch + kNoallocCounterSlot;
+  const bool nest = p.nesterov != 0;
+
+  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    const int r0 = (t / p.tiles_c) * kTileR, c0 = (t % p.tiles_c) * kTileC;
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < kTileR * kTileC; e += kStreamThreads) {
+      const int rr = e / kTileC, cc = e % kTileC;
+      const int r = r0 + rr, c = c0 + cc;
+      float u = 0.f;
+      if (r < p.rows && c < p.cols) {
+        const int64_t idx = (int64_t)r * p.cols + c;
+        const float g = GB ? __bfloat162float(reinterpret_cast<const bf16*>(p.grad)[idx])
+                           : reinterpret_cast<const float*>(p.grad)[idx];
+        const float mv = fmaf(p.mu, p.momentum[idx], g);
+        p.momentum[idx] = mv;
+        u = nest ? fmaf(p.mu, mv, g) : mv;
+        ss = fmaf(u, u, ss);
+      }
+      tileU[rr][cc] = u;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTileR * kTileC; e += kStreamThreads) {
+      // write in the short-side orientation: (r, c) as is, or (c, r) when rows > cols
+      int rr, cc;
+      if (p.transposed) {
+        cc = e / kTileR;
+        rr = e % kTileR;
+      } else {
+        rr = e / kTileC;
+        cc = e % kTileC;
+      }
+      const int r = r0 + rr, c = c0 + cc;
+      if (r >= p.rows || c >= p.cols) continue;
+      const int64_t o = p.transposed ? (int64_t)c * p.u_ld + r : (int64_t)r * p.u_ld + c;
+      if (XB)
+        reinterpret_cast<bf16*>(p.u)[o] = __float2bfloat16_rn(tileU[rr][cc]);
+      else
+        reinterpret_cast<float*>(p.u)[o] = tileU[rr][cc];
+    }
+    // per-tile partial, fixed-order block sum
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.f;
+      for (int k = 0; k < kStreamThreads / 32; ++k) b += red[k];
+      partial[t] = b;
+      __threadfence();
+      is_last = (atomicAdd(counter, 1u) == static_cast<unsigned>(p.n_tiles - 1));
+    }
+    __syncthreads();
+    if (is_last) {
+      __threadfence();
+      double acc = 0.0;
+      for (int k = threadIdx.x; k < p.n_tiles; k += kStreamThreads) acc += (double)__ldcg(&partial[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = acc;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int k = 0; k < kStreamThreads / 32; ++k) tot += redd[k];
+        *p.s_out = 1.0f / (static_cast<float>(sqrt(tot)) + p.eps);
+        *counter = 0u;  // leave the ticket at zero for the next call
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Device address of the static scratch, looked up once per device.
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+unsigned* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace dmuon
+
+using namespace dmuon;
+
+extern "C" dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* momentum, void* u_out, float* s_out,
+                                                    int64_t rows, int64_t cols, int32_t grad_dtype,
+                                                    int32_t u_dtype, float mu, int32_t nesterov, float eps,
+                                                    void* stream) {
+  if (grad == nullptr || momentum == nullptr || u_out == nullptr || s_out == nullptr)
+    return set_last_error(DMUON_ERR_INVALID_ARG, "NULL pointer argument");
+  if (rows < 1 || cols < 1 || rows > (1 << 20) || cols > (1 << 20) || rows * cols >= (1LL << 31))
+    return set_last_error(DMUON_ERR_INVALID_ARG, "unsupported matrix shape");
+  if ((grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16) || (u_dtype != DMUON_F32 && u_dtype != DMUON_BF16))
+    return set_last_error(DMUON_ERR_UNSUPPORTED, "grad and u dtypes must be DMUON_F32 or DMUON_BF16");
+  if (!std::isfinite(mu) || !(eps >= 0.f) || (nesterov != 0 && nesterov != 1))
+    return set_last_error(DMUON_ERR_INVALID_ARG, "bad mu, eps or nesterov");
+  const int64_t tiles_c = (cols + kTileC - 1) / kTileC;
+  const int64_t n_tiles = ((rows + kTileR - 1) / kTileR) * tiles_c;
+  if (n_tiles > kNoallocMaxUnits)
+    return set_last_error(DMUON_ERR_UNSUPPORTED,
+                          "matrix too large for the static scratch: ceil(rows/64)*ceil(cols/128) must be <= 65536");
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return set_last_error(DMUON_ERR_CUDA, "no usable current CUDA device");
+  unsigned* scratch;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      // The array's name in host code is only a host-side handle; the kernel
+      // needs its device address, fetched here with this device current.
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+        return set_last_error(DMUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+      g_scratch_addr[dev] = static_cast<unsigned*>(ptr);
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the ticket counter must start at zero, whatever an earlier call left behind
+  if (cudaMemsetAsync(scratch + kNoallocCounterSlot, 0, sizeof(unsigned), s) != cudaSuccess)
+    return set_last_error(DMUON_ERR_CUDA, "cudaMemsetAsync of the ticket counter failed");
+
+  NoallocParams p;
+  p.grad = grad;
+  p.momentum = momentum;
+  p.u = u_out;
+  p.s_out = s_out;
+  p.scratch = scratch;
+  p.rows = static_cast<int32_t>(rows);
+  p.cols = static_cast<int32_t>(cols);
+  p.transposed = rows > cols;
+  const int64_t n_long = rows > cols ? rows : cols;
+  p.u_ld = static_cast<int32_t>((n_long + 7) / 8 * 8);
+  p.tiles_c = static_cast<int32_t>(tiles_c);
+  p.n_tiles = static_cast<int32_t>(n_tiles);
+  p.mu = mu;
+  p.eps = eps;
+  p.nesterov = nesterov;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = static_cast<int>(std::min<int64_t>(n_tiles, 4LL * (sms > 0 ? sms : 1)));
+  const bool gb = grad_dtype == DMUON_BF16, xb = u_dtype == DMUON_BF16;
+  if (gb && xb)
+    momentum_norm_noalloc_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(p);
+  else if (gb)
+    momentum_norm_noalloc_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(p);
+  else if (xb)
+    momentum_norm_noalloc_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
+  else
+    momentum_norm_noalloc_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "kernel launch failed");
+  return set_last_error(DMUON_OK, "");
+}

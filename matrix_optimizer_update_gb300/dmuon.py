@@ -42,7 +42,8 @@ EXPORTS = (
     "dmuon_plan", "dmuon_plan_workspace_bytes", "dmuon_plan_bind", "dmuon_step",
     "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
     "dmuon_profile_begin", "dmuon_profile_end", "dmuon_launch_count",
-    "dmuon_selftest_wait_timeout", "dmuon_plan_destroy", "dmuon_last_error", "dmuon_version",
+    "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_plan_destroy", "dmuon_last_error",
+    "dmuon_version",
 )
 
 
@@ -88,6 +89,7 @@ def lib():
                                     i32, ctypes.POINTER(i32)]),
         "dmuon_launch_count": (i32, [vp, ctypes.POINTER(i64)]),
         "dmuon_selftest_wait_timeout": (i32, [vp, i64, vp, ctypes.POINTER(u32)]),
+        "dmuon_momentum_norm_noalloc": (i32, [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, f32, vp]),
         "dmuon_plan_destroy": (None, [vp]),
         "dmuon_last_error": (ctypes.c_char_p, []),
         "dmuon_version": (i32, []),
@@ -216,6 +218,15 @@ def dmuon_selftest_wait_timeout(d_scratch: int, limit_ns: int, stream: int = 0) 
     _check(lib().dmuon_selftest_wait_timeout(ctypes.c_void_p(d_scratch), int(limit_ns), ctypes.c_void_p(stream),
                                              ctypes.byref(b)))
     return b.value
+
+
+def dmuon_momentum_norm_noalloc(grad: int, momentum: int, u_out: int, s_out: int, rows: int, cols: int,
+                                grad_dtype="bf16", u_dtype="bf16", mu=0.95, nesterov=True, eps=1e-7, stream: int = 0):
+    """Momentum + normalisation pass of one matrix with no workspace (see include/dmuon.h)."""
+    _check(lib().dmuon_momentum_norm_noalloc(ctypes.c_void_p(grad), ctypes.c_void_p(momentum), ctypes.c_void_p(u_out),
+                                             ctypes.c_void_p(s_out), int(rows), int(cols), DTYPE[grad_dtype],
+                                             DTYPE[u_dtype], float(mu), int(bool(nesterov)), float(eps),
+                                             ctypes.c_void_p(stream)))
 
 
 @dataclass
