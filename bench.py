@@ -293,14 +293,15 @@ def run_ours(args):
         d["ms"] += kms
         d["work"] += work
         d["launches"] += 1
-    ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in ("gram", "poly", "gemm")) / args.steps
+    NS_KINDS = ("gram", "poly", "gemm", "symm")
+    ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in NS_KINDS) / args.steps
     peaks, peak_src = load_peaks()
     tensor_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    ns_kinds = {k: v for k, v in per_kind.items() if k in ("gram", "poly", "gemm")}
+    ns_kinds = {k: v for k, v in per_kind.items() if k in NS_KINDS}
     dom = max(ns_kinds, key=lambda k: ns_kinds[k]["ms"]) if ns_kinds else max(per_kind, key=lambda k: per_kind[k]["ms"])
     d = per_kind[dom]
-    if dom in ("gram", "poly", "gemm"):
+    if dom in NS_KINDS:
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved / tensor_peak, "peak_source": f"{peak_src} bf16_tflops_sustained",
@@ -314,7 +315,7 @@ def run_ours(args):
                 "traffic": traffic_for(dom, w.name)}
     kernels = {}
     for k, v in per_kind.items():
-        if k in ("gram", "poly", "gemm"):
+        if k in NS_KINDS:
             a = v["work"] / (v["ms"] * 1e-3) / 1e12
             kernels[k] = {"ms_per_step": v["ms"] / args.steps, "tflops": a, "frac_of_tensor_peak": a / tensor_peak}
         else:
@@ -322,30 +323,102 @@ def run_ours(args):
             kernels[k] = {"ms_per_step": v["ms"] / args.steps, "gbs": a, "frac_of_hbm_peak": a / hbm_peak,
                           "traffic": traffic_for(k, w.name)}
 
-    # ---- end to end: grads in from pinned host memory, updated weights out, every step
+    # ---- the Gram-space form of the iteration on the same matrix set (reported beside the headline)
+    gram = None
+    if not args.no_gram and w.compute == "bf16":
+        gm = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
+                            grad=w.grad_dtype, compute=w.compute, flags=dm.FLAG_GRAM_NS, device=f"cuda:{local}",
+                            stream=stream)
+        gplan = gm.plan
+        glps = len(gplan.describe()["launches"])
+        for _ in range(args.warmup):
+            gplan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
+        torch.cuda.synchronize()
+        barrier()
+        gplan.profile_begin(args.steps * glps)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            gplan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        gms = max_over_ranks(g0.elapsed_time(g1), world, f"cuda:{local}")
+        gprof = gplan.profile_end(args.steps * glps)
+        g_ns_ms = sum(kms for kind, kms, _ in gprof if dm.KIND_NAMES[kind] in NS_KINDS) / args.steps
+        g_ns_work = sum(wk for kind, _, wk in gprof if dm.KIND_NAMES[kind] in NS_KINDS) / args.steps
+        executed = g_ns_work / (g_ns_ms * 1e-3) / 1e12
+        gram = {"ms_per_step": gms / args.steps, "ns_ms_per_step": g_ns_ms,
+                "ns_flops_executed_per_step": g_ns_work,
+                "executed_tflops": executed, "executed_frac_of_peak": executed / tensor_peak,
+                "standard_equivalent_tflops": tot["ns_flops"] / (g_ns_ms * 1e-3) / 1e12,
+                "value": aggregate(tot["ns_flops"], args.steps, world, gms * 1e-3),
+                "launches_per_step": glps, "device_status": gplan.read_device_status(sh)}
+        del gm, gplan
+
+    # ---- end to end through the public API: every step copies that step's gradients in from pinned
+    # host memory, runs dmuon_step and reads the step's result (its 4-byte status word) back to the
+    # host, which also synchronises. The copy of step k+1's gradients (into a second device buffer,
+    # on a copy stream) overlaps step k. A second figure also copies every updated weight back out.
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(2, min(args.steps, 5))
         hG = torch.empty_like(ms.G, device="cpu", pin_memory=True)
-        hW = torch.empty_like(ms.W, device="cpu", pin_memory=True)
         hG.copy_(ms.G)
+        gbuf = [ms.G, torch.empty_like(ms.G)]
+        gptrs = [Gp, ms.ptrs(gbuf[1])]
+        copy_stream = torch.cuda.Stream()
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        used = [torch.cuda.Event(), torch.cuda.Event()]
         torch.cuda.synchronize()
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        t0 = time.perf_counter()
+        bits = 0
+        with torch.cuda.stream(copy_stream):
+            gbuf[0].copy_(hG, non_blocking=True)
+            copied[0].record(copy_stream)
+        for k in range(e2e_steps):
+            b = k & 1
+            if k + 1 < e2e_steps:  # upload the next step's gradients while this step runs
+                nb = (k + 1) & 1
+                with torch.cuda.stream(copy_stream):
+                    if k >= 1:
+                        copy_stream.wait_event(used[nb])
+                    gbuf[nb].copy_(hG, non_blocking=True)
+                    copied[nb].record(copy_stream)
+            stream.wait_event(copied[b])
+            plan.step(Wp, gptrs[b], Mp, w.lr, w.mu, w.nesterov, sh)
+            used[b].record(stream)
+            bits |= plan.read_device_status(sh)
+        torch.cuda.synchronize()
+        wall_ms = (time.perf_counter() - t0) * 1e3
+        barrier()
+        e2e_ms = max_over_ranks(wall_ms, world, f"cuda:{local}")
+        e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
+               "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+               "h2d_bytes_per_step": hG.numel() * hG.element_size(), "d2h_bytes_per_step": 4,
+               "result_read": "device status word (dmuon_read_device_status), every step",
+               "timing": "host wall clock from the first upload to the last status read",
+               "overlap": "next step's gradient upload overlaps the current step (two device buffers)",
+               "device_status": bits}
+        del gbuf[1]
+        hW = torch.empty_like(ms.W, device="cpu", pin_memory=True)
+        torch.cuda.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
         with torch.cuda.stream(stream):
             for _ in range(e2e_steps):
                 ms.G.copy_(hG, non_blocking=True)
                 step()
                 hW.copy_(ms.W, non_blocking=True)
-        e1.record(stream)
+        f1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, f"cuda:{local}")
-        e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
-               "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
-               "h2d_bytes_per_step": hG.numel() * hG.element_size(),
-               "d2h_bytes_per_step": hW.numel() * hW.element_size()}
+        full_ms = max_over_ranks(f0.elapsed_time(f1), world, f"cuda:{local}")
+        e2e["with_weight_readback"] = {"value": aggregate(tot["ns_flops"], e2e_steps, world, full_ms * 1e-3),
+                                       "ms_per_step": full_ms / e2e_steps,
+                                       "d2h_bytes_per_step": hW.numel() * hW.element_size()}
         del hG, hW
 
     cpu = None
@@ -367,7 +440,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
         "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
-        "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "kernels": kernels, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches,
         "clocks": clk, "device_status": status,
     }
     if rank == 0:
@@ -390,6 +464,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="truncate the workload to its first N layers (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
     if args.impl == "reference":

@@ -81,6 +81,20 @@ typedef struct {
 /* Plan flags. */
 #define DMUON_FLAG_CAPTURE_UPDATE 0x1u /* keep the fp32 update X of the last step
                                           (read it with dmuon_read_update)      */
+#define DMUON_FLAG_GRAM_NS 0x2u        /* matrices with max(rows,cols) > min(rows,cols)
+                                          iterate in the m x m Gram space: G = X X^T
+                                          once, then per step P = aI + bG + cG^2,
+                                          Q <- P Q, G <- P G P; finally X = Q X0
+                                          ("DMuon: Efficient Distributed Muon
+                                          Training with Near-Adam Overhead",
+                                          gist.science summary section 2, "Gram
+                                          Space Recurrence"). Fewer flops when the
+                                          matrix is wide; square ones keep the
+                                          standard form.                         */
+#define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
+                                          per bucket on the bound workspace, keep
+                                          the faster, and order tiles by measured
+                                          time (see dmuon_plan_costs). bf16 only. */
 
 /* Device status bits (dmuon_read_device_status). */
 #define DMUON_DEV_NONFINITE_NORM 0x1u  /* ||U||_F was NaN or Inf for some matrix  */
@@ -93,6 +107,8 @@ typedef struct {
 #define DMUON_KIND_POLY 2     /* B = b*A + c*A A^T, upper tiles, mirrored          */
 #define DMUON_KIND_GEMM 3     /* X' = a*X + B X (last step: W update epilogue)     */
 #define DMUON_KIND_UPDATE0 4  /* W update straight from U (ns_steps == 0)          */
+#define DMUON_KIND_SYMM 5     /* Gram-space form: product of two commuting
+                                 symmetric m x m matrices, upper tiles, mirrored   */
 
 typedef struct dmuon_plan_s* dmuon_plan_t;
 
@@ -153,8 +169,10 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  * pointers differs from the previous call's it is uploaded with a
  * cudaMemcpyAsync from host memory; under CUDA-graph capture, make one
  * uncaptured call with the same pointers first so that none is needed.
- * Launches 1 + 3*ns_steps kernels (1 + 1 when ns_steps == 0; more when the
- * plan has more than 8 buckets).
+ * Launches one momentum kernel, then 3*ns_steps kernels per chunk of
+ * standard-form buckets and 4*ns_steps - 1 per chunk of Gram-space buckets
+ * (a chunk: up to 8 buckets sharing form and tile widths); 1 + 1 kernels
+ * when ns_steps == 0. dmuon_plan_describe lists them.
  */
 dmuon_status dmuon_step(dmuon_plan_t plan, void* const* params, const void* const* grads,
                         void* const* momenta, float lr, float mu, int32_t nesterov, void* stream);
@@ -194,6 +212,18 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t plan, char* buf, size_t len, size_
 dmuon_status dmuon_profile_begin(dmuon_plan_t plan, int32_t max_launches);
 dmuon_status dmuon_profile_end(dmuon_plan_t plan, int32_t* kinds, float* ms, double* work,
                                int32_t cap, int32_t* n);
+
+/*
+ * dmuon_plan_costs - predicted GPU milliseconds of each matrix's
+ * Newton-Schulz work (its tiles times the measured time per tile, spread over
+ * all SMs), from the timings a DMUON_FLAG_TUNE bind made. n must equal the
+ * plan's matrix count; per_matrix_ms is a host array. Returns
+ * DMUON_ERR_UNSUPPORTED for a plan that was not tuned. The costs can be
+ * passed to dmuon_assign_owners ("DMuon: Efficient Distributed Muon Training
+ * with Near-Adam Overhead", gist.science summary section 2.3: owners are
+ * balanced on measured, not theoretical, costs).
+ */
+dmuon_status dmuon_plan_costs(dmuon_plan_t plan, double* per_matrix_ms, int32_t n);
 
 /* Number of kernels the library has launched through this plan so far. */
 dmuon_status dmuon_launch_count(dmuon_plan_t plan, int64_t* count);
@@ -239,6 +269,49 @@ dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void
 dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* momentum, void* u_out, float* s_out,
                                          int64_t rows, int64_t cols, int32_t grad_dtype, int32_t u_dtype,
                                          float mu, int32_t nesterov, float eps, void* stream);
+
+/*
+ * dmuon_assign_owners - choose one owner rank for every matrix so that the
+ * largest predicted per-rank load is small ("DMuon: Efficient Distributed
+ * Muon Training with Near-Adam Overhead", gist.science summary section 2.1:
+ * one owner per matrix runs its update; section 2.3: minimise the predicted
+ * makespan over owner ranks, greedy when the search space is large).
+ *
+ *  shapes[n_mats]   stored shapes (host).
+ *  ns_steps         0..16; with costs == NULL the cost of a matrix is its
+ *                   Newton-Schulz flops (symmetric products counted once;
+ *                   ns_steps 0 counts as 1).
+ *  costs            optional host array of n_mats finite costs >= 0 (e.g.
+ *                   measured times); NULL = the flop count above.
+ *  n_ranks          >= 1.
+ *  owner_out        host array of n_mats: the owner rank of each matrix.
+ *  load_out         optional host array of n_ranks: the summed cost per rank.
+ *
+ * Longest-processing-time-first greedy, then moves and swaps out of the
+ * most-loaded rank while they lower the makespan. Deterministic: every rank
+ * that calls it with the same arguments gets the same assignment. Host only.
+ */
+dmuon_status dmuon_assign_owners(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_steps,
+                                 const double* costs, int32_t n_ranks, int32_t* owner_out,
+                                 double* load_out);
+
+/*
+ * dmuon_adamw_flat - one AdamW step over a flat buffer of n elements, for the
+ * parameters the Muon predicate leaves out ("DMuon" project docs, section
+ * "DMuon 能做什么": everything else is optimised by AdamW with its own
+ * learning rate, adamw_lr). Decoupled weight decay and bias correction:
+ *   p <- p*(1 - lr*wd);  m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g^2
+ *   p <- p - lr/(1-b1^t) * m / (sqrt(v)/sqrt(1-b2^t) + eps)
+ *
+ *  param        device, n elements of param_dtype (DMUON_F32/DMUON_BF16), in place.
+ *  grad         device, n elements of grad_dtype, read only.
+ *  exp_avg, exp_avg_sq  device, n fp32 each (m and v), in place.
+ *  step         t >= 1 (the step being taken); 0 <= beta1, beta2 < 1; eps >= 0.
+ * All four pointers 16-byte aligned. One kernel on stream; no allocation.
+ */
+dmuon_status dmuon_adamw_flat(void* param, const void* grad, float* exp_avg, float* exp_avg_sq, int64_t n,
+                              int32_t param_dtype, int32_t grad_dtype, float lr, float beta1, float beta2,
+                              float eps, float weight_decay, int32_t step, void* stream);
 
 /* Free the host-side plan (the workspace stays the caller's). NULL is a no-op. */
 void dmuon_plan_destroy(dmuon_plan_t plan);

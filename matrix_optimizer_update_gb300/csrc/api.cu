@@ -21,6 +21,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <string>
 #include <vector>
 
@@ -48,16 +49,27 @@ dmuon_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int64_t kAlign = 1024;
+constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace buffers of a bucket, by role. Standard buckets use X0/X1 (the
+// iterate, ping-pong), A and B; Gram-space buckets use X0 (U, read twice), G,
+// P, Q0/Q1 (ping-pong) and R.
+enum BufRole : int { kBufNone = -1, kBufX0 = 0, kBufX1, kBufA, kBufB, kBufQ0, kBufQ1, kBufR, kBufCount };
 
 struct BucketPlan {
   int32_t m = 0, n = 0, count = 0, n_transposed = 0;
   int32_t x_ld = 0, m_ld = 0;
+  bool gram = false;          // iterate in the m x m Gram space
+  int32_t bn_sym = 0;         // tile width of the symmetric products (m x m outputs)
+  int32_t bn_gemm = 0;        // tile width of the m x n product
+  double tile_ms[3] = {0, 0, 0};  // measured ms per tile: X X^T (K = n), m x m products, gemm; 0 = not measured
   std::vector<int32_t> mats;  // slot -> global matrix index
   int64_t off_slotmat = -1;
-  int64_t off_x[2] = {-1, -1}, off_a = -1, off_b = -1;
+  int64_t off[kBufCount] = {-1, -1, -1, -1, -1, -1, -1};
   int64_t x_mat_bytes = 0, a_mat_bytes = 0;
+  bool is_x(int role) const { return role == kBufX0 || role == kBufX1; }
 };
 
 struct ListRef {
@@ -65,10 +77,18 @@ struct ListRef {
   int32_t count = 0;
 };
 
+enum ListKind : int { kListGram = 0, kListPoly = 1, kListGemm = 2 };
+
 struct Launch {
   int kind = 0;   // DMUON_KIND_*
+  int phase = 0;  // kernel: kPhaseGram / kPhasePoly / kPhaseGemm
   int step = -1;  // Newton-Schulz step
   int chunk = 0;
+  int list = 0;   // ListKind
+  int bn = 0;     // tile width of this launch
+  int opA = kBufNone, opB = kBufNone, out = kBufNone, aux = kBufNone;
+  float a = 0.f, b = 0.f, c = 0.f, diag = 0.f;
+  int first = 0, last = 0;
   int32_t grid = 0;
   double work = 0;  // algorithmic flops (products) or bytes (streaming)
   int param_index = -1;
@@ -106,13 +126,14 @@ struct dmuon_plan_s {
   int64_t n_units = 0;
   std::vector<BucketPlan> buckets;
   std::vector<std::vector<int>> chunks;
+  std::vector<bool> chunk_gram;
   std::vector<int4> items;
   std::vector<ListRef> gram_lists, poly_lists, gemm_lists;
   std::vector<Launch> launches;
   // ---- workspace layout (byte offsets)
   size_t ws_bytes = 0;
   int64_t off_status = 0, off_counters = 0, off_s = 0, off_partial = 0, off_mats = 0, off_ub = 0, off_ptrs = 0,
-          off_items = 0, off_capture = -1;
+          off_items = 0, off_probe = 0, off_capture = -1;
   int64_t cap_elems = 0;
   // ---- binding
   char* ws = nullptr;
@@ -132,6 +153,7 @@ struct dmuon_plan_s {
   std::vector<int32_t> prof_kind;
   std::vector<double> prof_work;
   int64_t launch_count = 0;
+  bool tuned = false;
 };
 
 namespace {
@@ -141,6 +163,7 @@ double phase_flops(int kind, double m, double n) {
     case DMUON_KIND_GRAM:
       return m * (m + 1) * n;
     case DMUON_KIND_POLY:
+    case DMUON_KIND_SYMM:
       return m * m * (m + 1);
     case DMUON_KIND_GEMM:
       return 2 * m * m * n;
@@ -151,9 +174,16 @@ double phase_flops(int kind, double m, double n) {
 
 int dtype_bytes(int32_t d) { return d == DMUON_BF16 ? 2 : 4; }
 
+// Default tile width for an output dimension of extent d: 256, unless the last
+// 256-wide tile would be at most half full, then 128.
+int32_t default_bn(int d) {
+  const int rem = d % 256;
+  return (rem != 0 && rem <= 128) ? 128 : 256;
+}
+
 // Tiles of one phase for one bucket, appended in cost order.
 void add_tiles(const dmuon_plan_s& P, int kind, int bucket_local, const BucketPlan& B, std::vector<int4>& out) {
-  const int BM = P.tile_m, BN = P.tile_n;
+  const int BM = P.tile_m, BN = (kind == DMUON_KIND_GEMM) ? B.bn_gemm : B.bn_sym;
   const int tm = static_cast<int>(cdiv(B.m, BM));
   if (kind == DMUON_KIND_GEMM) {
     const int tn = static_cast<int>(cdiv(B.n, BN));
@@ -169,6 +199,9 @@ void add_tiles(const dmuon_plan_s& P, int kind, int bucket_local, const BucketPl
   }
 }
 
+dmuon_status finish_plan(dmuon_plan_s& P);
+
+// Buckets (with default tile widths), per-matrix tables and streaming units.
 dmuon_status build_plan(dmuon_plan_s& P) {
   const int n_mats = static_cast<int>(P.shapes.size());
   P.tc = (P.dt.compute == DMUON_BF16);
@@ -198,6 +231,9 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].n = order[b].second;
     P.buckets[b].x_ld = static_cast<int32_t>(align_up(order[b].second, ld_mult));
     P.buckets[b].m_ld = static_cast<int32_t>(align_up(order[b].first, ld_mult));
+    P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second > order[b].first;
+    P.buckets[b].bn_sym = P.tc ? default_bn(order[b].first) : kSimtBN;
+    P.buckets[b].bn_gemm = P.tc ? default_bn(order[b].second) : kSimtBN;
   }
 
   P.mats.assign(n_mats, MatDev{});
@@ -235,13 +271,45 @@ dmuon_status build_plan(dmuon_plan_s& P) {
   P.unit_begin[n_mats] = units;
   P.n_units = units;
   P.cap_elems = cap;
+  return finish_plan(P);
+}
 
-  // ---- launch chunks of at most kMaxBucketsPerLaunch buckets
+// Tile widths, launch chunks, cost-ordered tile lists, workspace layout and
+// launch sequence. Called again after tuning changes tile widths or costs;
+// the workspace layout does not move (the tile-list region is sized for the
+// largest possible lists).
+dmuon_status finish_plan(dmuon_plan_s& P) {
+  const int n_mats = static_cast<int>(P.shapes.size());
+  const int64_t units = P.n_units, cap = P.cap_elems;
+
+  // ---- launch chunks: at most kMaxBucketsPerLaunch buckets sharing iteration form and tile widths
   P.chunks.clear();
-  for (size_t b = 0; b < P.buckets.size(); b += kMaxBucketsPerLaunch) {
-    std::vector<int> ch;
-    for (size_t q = b; q < std::min(P.buckets.size(), b + kMaxBucketsPerLaunch); ++q) ch.push_back((int)q);
-    P.chunks.push_back(ch);
+  P.chunk_gram.clear();
+  {
+    std::vector<std::tuple<int, int, int>> keys;
+    for (const BucketPlan& B : P.buckets) {
+      const auto k = std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm);
+      if (std::find(keys.begin(), keys.end(), k) == keys.end()) keys.push_back(k);
+    }
+    std::stable_sort(keys.begin(), keys.end(),
+                     [](const auto& a, const auto& b) { return std::get<0>(a) < std::get<0>(b); });
+    for (const auto& k : keys) {
+      std::vector<int> ch;
+      for (size_t b = 0; b < P.buckets.size(); ++b) {
+        const BucketPlan& B = P.buckets[b];
+        if (std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm) != k) continue;
+        ch.push_back(static_cast<int>(b));
+        if (ch.size() == kMaxBucketsPerLaunch) {
+          P.chunks.push_back(ch);
+          P.chunk_gram.push_back(std::get<0>(k) != 0);
+          ch.clear();
+        }
+      }
+      if (!ch.empty()) {
+        P.chunks.push_back(ch);
+        P.chunk_gram.push_back(std::get<0>(k) != 0);
+      }
+    }
   }
 
   // ---- cost-ordered tile lists per (phase, chunk)
@@ -252,7 +320,9 @@ dmuon_status build_plan(dmuon_plan_s& P) {
       const BucketPlan& B = P.buckets[ch[lb]];
       std::vector<int4> t;
       add_tiles(P, kind, static_cast<int>(lb), B, t);
-      const double cost = (kind == DMUON_KIND_GRAM) ? B.n : B.m;  // K extent of every tile
+      // cost of one tile: its measured time when the plan was tuned, else its K extent
+      const int li = (kind == DMUON_KIND_GRAM) ? 0 : (kind == DMUON_KIND_POLY) ? 1 : 2;
+      const double cost = B.tile_ms[li] > 0 ? B.tile_ms[li] * 1e9 : (kind == DMUON_KIND_GRAM) ? B.n : B.m;
       for (const int4& v : t) tmp.push_back({cost, v});
     }
     std::stable_sort(tmp.begin(), tmp.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
@@ -287,21 +357,44 @@ dmuon_status build_plan(dmuon_plan_s& P) {
   P.off_mats = take((int64_t)sizeof(MatDev) * n_mats);
   P.off_ub = take(8LL * (n_mats + 1));
   P.off_ptrs = take(8LL * 3 * n_mats);
-  P.off_items = take((int64_t)sizeof(int4) * std::max<size_t>(P.items.size(), 1));
+  // tile lists: room for the longest lists any choice of tile widths gives (all 128 wide)
+  int64_t cap_items = 0;
+  if (P.ns_steps > 0) {
+    for (const BucketPlan& B : P.buckets) {
+      const int64_t tm = cdiv(B.m, P.tile_m), bn = P.tc ? 128 : kSimtBN;
+      int64_t sym = 0;
+      for (int64_t ti = 0; ti < tm; ++ti)
+        for (int64_t tj = 0; tj < cdiv(B.m, bn); ++tj)
+          if (tj * bn + bn - 1 >= ti * P.tile_m) ++sym;
+      cap_items += B.count * (2 * sym + tm * cdiv(B.n, bn));
+    }
+  }
+  P.off_items = take((int64_t)sizeof(int4) * std::max<int64_t>(std::max<int64_t>(cap_items, (int64_t)P.items.size()), 1));
+  P.off_probe = take((int64_t)sizeof(int4) * kProbeTiles);
   for (BucketPlan& B : P.buckets) {
     B.off_slotmat = take(4LL * B.count);
     B.x_mat_bytes = (int64_t)B.m * B.x_ld * P.xel;
     B.a_mat_bytes = (int64_t)B.m * B.m_ld * P.xel;
-    B.off_x[0] = take(B.x_mat_bytes * B.count);
-    B.off_x[1] = (P.ns_steps >= 2) ? take(B.x_mat_bytes * B.count) : -1;
-    if (P.ns_steps >= 1) {
-      B.off_a = take(B.a_mat_bytes * B.count);
-      B.off_b = take(B.a_mat_bytes * B.count);
+    B.off[kBufX0] = take(B.x_mat_bytes * B.count);
+    if (!B.gram) {
+      if (P.ns_steps >= 2) B.off[kBufX1] = take(B.x_mat_bytes * B.count);
+      if (P.ns_steps >= 1) {
+        B.off[kBufA] = take(B.a_mat_bytes * B.count);
+        B.off[kBufB] = take(B.a_mat_bytes * B.count);
+      }
+    } else {
+      B.off[kBufA] = take(B.a_mat_bytes * B.count);   // G
+      B.off[kBufQ0] = take(B.a_mat_bytes * B.count);  // P_0 = Q_1, then every other Q
+      if (P.ns_steps >= 2) {
+        B.off[kBufB] = take(B.a_mat_bytes * B.count);   // P_k, k >= 1
+        B.off[kBufQ1] = take(B.a_mat_bytes * B.count);
+        B.off[kBufR] = take(B.a_mat_bytes * B.count);   // P_k G_k
+      }
     }
   }
   for (int i = 0; i < n_mats; ++i) {
     const BucketPlan& B = P.buckets[P.mats[i].bucket];
-    P.mats[i].x0_off = B.off_x[0] + (int64_t)P.mats[i].slot * B.x_mat_bytes;
+    P.mats[i].x0_off = B.off[kBufX0] + (int64_t)P.mats[i].slot * B.x_mat_bytes;
   }
   P.off_capture = (P.flags & DMUON_FLAG_CAPTURE_UPDATE) ? take(4 * std::max<int64_t>(cap, 1)) : -1;
   P.ws_bytes = static_cast<size_t>(off);
@@ -321,20 +414,65 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     u.work = elems * (2 * pb + P.xel);
     P.launches.push_back(u);
   }
-  for (int k = 0; k < P.ns_steps; ++k) {
-    for (int kind : {DMUON_KIND_GRAM, DMUON_KIND_POLY, DMUON_KIND_GEMM}) {
-      for (size_t c = 0; c < P.chunks.size(); ++c) {
-        Launch x;
-        x.kind = kind;
-        x.step = k;
-        x.chunk = static_cast<int>(c);
-        for (int b : P.chunks[c]) {
-          const BucketPlan& B = P.buckets[b];
-          x.work += B.count * phase_flops(kind, B.m, B.n);
-        }
-        P.launches.push_back(x);
+  auto add = [&](int kind, int phase, int step, int chunk, int list, int opA, int opB, int out, int aux, float a,
+                 float b, float c, float diag, int first, int last) {
+    Launch x;
+    x.kind = kind;
+    x.phase = phase;
+    x.step = step;
+    x.chunk = chunk;
+    x.list = list;
+    x.bn = (phase == kPhaseGemm) ? P.buckets[P.chunks[chunk][0]].bn_gemm : P.buckets[P.chunks[chunk][0]].bn_sym;
+    x.opA = opA;
+    x.opB = opB;
+    x.out = out;
+    x.aux = aux;
+    x.a = a;
+    x.b = b;
+    x.c = c;
+    x.diag = diag;
+    x.first = first;
+    x.last = last;
+    for (int bi : P.chunks[chunk]) {
+      const BucketPlan& B = P.buckets[bi];
+      x.work += B.count * phase_flops(kind, B.m, B.n);
+    }
+    P.launches.push_back(x);
+  };
+  const int S = P.ns_steps;
+  auto cf = [&](int k, int q) { return P.coeffs[3 * k + q]; };
+  // standard form, step by step: A = X X^T; B = b A + c A A^T; X' = a X + B X (last: W update)
+  for (int k = 0; k < S; ++k) {
+    const int xin = (k & 1) ? kBufX1 : kBufX0, xout = (k & 1) ? kBufX0 : kBufX1;
+    for (size_t ch = 0; ch < P.chunks.size(); ++ch)
+      if (!P.chunk_gram[ch])
+        add(DMUON_KIND_GRAM, kPhaseGram, k, (int)ch, kListGram, xin, xin, kBufA, kBufNone, 0, 0, 0, 0, k == 0, 0);
+    for (size_t ch = 0; ch < P.chunks.size(); ++ch)
+      if (!P.chunk_gram[ch])
+        add(DMUON_KIND_POLY, kPhasePoly, k, (int)ch, kListPoly, kBufA, kBufA, kBufB, kBufA, 0, cf(k, 1), cf(k, 2),
+            0, 0, 0);
+    for (size_t ch = 0; ch < P.chunks.size(); ++ch)
+      if (!P.chunk_gram[ch])
+        add(DMUON_KIND_GEMM, kPhaseGemm, k, (int)ch, kListGemm, kBufB, xin, k == S - 1 ? kBufNone : xout, xin,
+            cf(k, 0), 0, 0, 0, k == 0, k == S - 1);
+  }
+  // Gram-space form: G = X0 X0^T; per step P = a I + b G + c G^2, Q <- P Q, G <- (P G) P; X = Q X0
+  for (size_t ch = 0; ch < P.chunks.size(); ++ch) {
+    if (!P.chunk_gram[ch]) continue;
+    const int c = static_cast<int>(ch);
+    add(DMUON_KIND_GRAM, kPhaseGram, 0, c, kListGram, kBufX0, kBufX0, kBufA, kBufNone, 0, 0, 0, 0, 1, 0);
+    auto qbuf = [](int j) { return (j & 1) ? kBufQ1 : kBufQ0; };  // Q_k lives in qbuf(k + 1), k >= 1
+    for (int k = 0; k < S; ++k) {
+      const int pk = (k == 0) ? kBufQ0 : kBufB;
+      add(DMUON_KIND_POLY, kPhasePoly, k, c, kListPoly, kBufA, kBufA, pk, kBufA, 0, cf(k, 1), cf(k, 2), cf(k, 0), 0,
+          0);
+      if (k >= 1) add(DMUON_KIND_SYMM, kPhaseGram, k, c, kListPoly, pk, qbuf(k + 1), qbuf(k), kBufNone, 0, 0, 0, 0, 0, 0);
+      if (k < S - 1) {
+        add(DMUON_KIND_SYMM, kPhaseGram, k, c, kListPoly, pk, kBufA, kBufR, kBufNone, 0, 0, 0, 0, 0, 0);
+        add(DMUON_KIND_SYMM, kPhaseGram, k, c, kListPoly, kBufR, pk, kBufA, kBufNone, 0, 0, 0, 0, 0, 0);
       }
     }
+    add(DMUON_KIND_GEMM, kPhaseGemm, S - 1, c, kListGemm, qbuf(S + 1), kBufX0, kBufNone, kBufX0, 0.f, 0, 0, 0, 1, 1);
   }
   return DMUON_OK;
 }
@@ -351,6 +489,54 @@ dmuon_status make_map(CUtensorMap* map, const void* base, int inner, int rows, i
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DMUON_OK;
+}
+
+// A bucket buffer seen as [count][rows][inner] with row pitch ld.
+struct View {
+  char* base;
+  int inner, rows, ld;
+  int64_t mat_bytes;
+};
+
+View view_of(const dmuon_plan_s& P, const BucketPlan& B, int role) {
+  View v{nullptr, 0, 0, 0, 0};
+  if (role == kBufNone || B.off[role] < 0) return v;
+  v.base = P.ws + B.off[role];
+  v.rows = B.m;
+  if (B.is_x(role)) {
+    v.inner = B.n;
+    v.ld = B.x_ld;
+    v.mat_bytes = B.x_mat_bytes;
+  } else {
+    v.inner = B.m;
+    v.ld = B.m_ld;
+    v.mat_bytes = B.a_mat_bytes;
+  }
+  return v;
+}
+
+// Operand maps and epilogue pointers of one bucket for one tensor-core launch.
+dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phase, int bn, int opA, int opB,
+                            int out, int aux, TcBucket& tb) {
+  tb.slot_mat = reinterpret_cast<const int32_t*>(P.ws + B.off_slotmat);
+  tb.m = B.m;
+  tb.n = B.n;
+  const View va = view_of(P, B, opA), vb = view_of(P, B, opB), vo = view_of(P, B, out), vx = view_of(P, B, aux);
+  dmuon_status st = make_map(&tb.tmA, va.base, va.inner, va.rows, B.count, va.ld, 64, kTcBM);
+  if (st != DMUON_OK) return st;
+  if (phase == kPhaseGemm)  // the m x n operand, MN-major: 64 columns x 64 rows per box
+    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, 64);
+  else
+    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bn);
+  if (st != DMUON_OK) return st;
+  tb.kdim = (phase == kPhaseGemm) ? B.m : va.inner;
+  tb.out = vo.base;
+  tb.out_mat_stride = vo.mat_bytes;
+  tb.out_ld = vo.ld;
+  tb.aux = vx.base;
+  tb.aux_mat_stride = vx.mat_bytes;
+  tb.aux_ld = vx.ld;
   return DMUON_OK;
 }
 
@@ -377,6 +563,104 @@ void destroy_events(dmuon_plan_s& P) {
   P.prof_max = P.prof_n = 0;
 }
 
+// Init-time tuning (DMUON_FLAG_TUNE): for every bucket and both tile widths,
+// time a GPU-filling slice of its X X^T tiles (K = n), of its m x m products
+// (K = m) and of its gemm tiles on the bound workspace (results discarded),
+// keep the faster width per kind of product, and record the measured time per
+// tile, which then orders the tile lists and feeds dmuon_plan_costs. This is
+// the single-GPU form of the pages' initialisation profiling of kernel
+// schedules per matrix shape (gist.science summary section 2.3, "Profiling";
+// section 2.4: the chosen configuration is cached and reused).
+dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e;
+  if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    return cuda_fail(e, "cudaEventCreate");
+  }
+  dmuon_status st = DMUON_OK;
+  int4* probe = reinterpret_cast<int4*>(P.ws + P.off_probe);
+  std::vector<int4> tiles;
+  const int bns[2] = {128, 256};
+  for (BucketPlan& B : P.buckets) {
+    double tms[2][3] = {{0, 0, 0}, {0, 0, 0}};
+    int64_t per_mat[2][2] = {{0, 0}, {0, 0}};
+    for (int bi = 0; bi < 2 && st == DMUON_OK; ++bi) {
+      BucketPlan T = B;
+      T.bn_sym = T.bn_gemm = bns[bi];
+      for (int kind = 0; kind < 3 && st == DMUON_OK; ++kind) {
+        tiles.clear();
+        add_tiles(P, kind == 2 ? DMUON_KIND_GEMM : DMUON_KIND_GRAM, 0, T, tiles);
+        per_mat[bi][kind == 2 ? 1 : 0] = static_cast<int64_t>(tiles.size()) / B.count;
+        const int n = static_cast<int>(std::min<int64_t>({(int64_t)tiles.size(), 4LL * P.num_sms, kProbeTiles}));
+        if ((e = cudaMemcpyAsync(probe, tiles.data(), sizeof(int4) * n, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+            (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+          st = cuda_fail(e, "probe upload");
+          break;
+        }
+        int phase, opA, opB, out, aux = kBufNone;
+        if (kind == 0) {
+          phase = kPhaseGram, opA = opB = kBufX0, out = kBufA;
+        } else if (kind == 1) {
+          phase = kPhaseGram, opA = opB = kBufA, out = B.off[kBufB] >= 0 ? kBufB : kBufQ0;
+        } else {
+          // writes over its own operand: the values are garbage, only the time is used
+          phase = kPhaseGemm, opA = kBufA, opB = kBufX0, out = kBufX0, aux = kBufX0;
+        }
+        TcParams tp;
+        std::memset(&tp, 0, sizeof(tp));
+        if ((st = fill_tc_bucket(P, T, phase, bns[bi], opA, opB, out, aux, tp.bk[0])) != DMUON_OK) break;
+        tp.items = probe;
+        tp.n_items = n;
+        tp.a = 1.f;
+        tp.mats = P.sp.mats;
+        tp.ptrs = P.sp.ptrs;
+        tp.s_norm = P.sp.s_norm;
+        tp.status = P.sp.status;
+        tp.param_bf16 = P.sp.param_bf16;
+        tp.timeout_ns = 2000000000LL;
+        const int grid = std::max(1, std::min(n, P.num_sms));
+        float ms = 0.f;
+        if ((e = launch_tc(phase, bns[bi], tp, grid, s)) != cudaSuccess || (e = cudaEventRecord(e0, s)) != cudaSuccess) {
+          st = cuda_fail(e, "tuning launch");
+          break;
+        }
+        for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) e = launch_tc(phase, bns[bi], tp, grid, s);
+        if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+        if (e != cudaSuccess) {
+          st = cuda_fail(e, "tuning run");
+          break;
+        }
+        const int waves = (n + grid - 1) / grid;
+        tms[bi][kind] = ms / 3.0 / waves;
+      }
+    }
+    if (st != DMUON_OK) break;
+    const double S = P.ns_steps;
+    const double n_xx = B.gram ? 1.0 : S, n_mm = B.gram ? 4.0 * S - 3.0 : S, n_gm = B.gram ? 1.0 : S;
+    int bs = 1, bg = 1;
+    double best_s = 1e300, best_g = 1e300;
+    for (int bi = 0; bi < 2; ++bi) {
+      const double cs = per_mat[bi][0] * (n_xx * tms[bi][0] + n_mm * tms[bi][1]);
+      const double cg = per_mat[bi][1] * n_gm * tms[bi][2];
+      if (cs < best_s) best_s = cs, bs = bi;
+      if (cg < best_g) best_g = cg, bg = bi;
+    }
+    B.bn_sym = bns[bs];
+    B.bn_gemm = bns[bg];
+    B.tile_ms[0] = tms[bs][0];
+    B.tile_ms[1] = tms[bs][1];
+    B.tile_ms[2] = tms[bg][2];
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != DMUON_OK) return st;
+  P.tuned = true;
+  return finish_plan(P);
+}
+
 }  // namespace
 
 dmuon_status dmuon::set_last_error(dmuon_status st, const char* msg) {
@@ -400,7 +684,8 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (shapes == nullptr || n_mats <= 0) return fail(DMUON_ERR_INVALID_ARG, "empty matrix list");
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
-  if (flags & ~DMUON_FLAG_CAPTURE_UPDATE) return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
+  if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE))
+    return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
   if (dtypes.momentum != DMUON_F32) return fail(DMUON_ERR_UNSUPPORTED, "momentum must be DMUON_F32");
@@ -509,74 +794,46 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   sp.x_bf16 = P->tc;
   sp.param_bf16 = P->dt.param == DMUON_BF16;
 
+  // init-time tuning of tile widths and per-tile costs (needs the tables and sp above)
+  if ((P->flags & DMUON_FLAG_TUNE) && P->tc && P->ns_steps > 0) {
+    dmuon_status st = tune_plan(*P, s);
+    if (st != DMUON_OK) return st;
+    if ((e = up(P->off_items, P->items.data(), sizeof(int4) * P->items.size())) != cudaSuccess ||
+        (e = cudaMemsetAsync(ws + P->off_status, 0, 4, s)) != cudaSuccess || (e = cudaStreamSynchronize(s)) != cudaSuccess)
+      return cuda_fail(e, "tuned table upload");
+  }
+
   // per-launch kernel parameters
   P->tc_params.clear();
   P->simt_params.clear();
   const int4* items = reinterpret_cast<const int4*>(ws + P->off_items);
   for (Launch& L : P->launches) {
     if (L.kind == DMUON_KIND_MOMENTUM || L.kind == DMUON_KIND_UPDATE0) {
-      L.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(P->n_units, 4LL * P->num_sms)));
+      const int per_sm = (L.kind == DMUON_KIND_MOMENTUM) ? momentum_blocks_per_sm(sp.grad_bf16, sp.x_bf16) : 4;
+      L.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(P->n_units, (int64_t)per_sm * P->num_sms)));
       continue;
     }
-    const int k = L.step;
     const std::vector<int>& ch = P->chunks[L.chunk];
-    const ListRef& lr = (L.kind == DMUON_KIND_GRAM)   ? P->gram_lists[L.chunk]
-                        : (L.kind == DMUON_KIND_POLY) ? P->poly_lists[L.chunk]
-                                                      : P->gemm_lists[L.chunk];
-    const int xin = k & 1, xout = (k + 1) & 1;
-    const bool first = (k == 0), last = (k == P->ns_steps - 1);
-    const float a = P->coeffs[3 * k], b = P->coeffs[3 * k + 1], c = P->coeffs[3 * k + 2];
+    const ListRef& lr = (L.list == kListGram)   ? P->gram_lists[L.chunk]
+                        : (L.list == kListPoly) ? P->poly_lists[L.chunk]
+                                                : P->gemm_lists[L.chunk];
+    auto view = [&](const BucketPlan& B, int role) { return view_of(*P, B, role); };
     if (P->tc) {
       TcParams tp;
       std::memset(&tp, 0, sizeof(tp));
       for (size_t lb = 0; lb < ch.size(); ++lb) {
         const BucketPlan& B = P->buckets[ch[lb]];
-        TcBucket& tb = tp.bk[lb];
-        tb.slot_mat = reinterpret_cast<const int32_t*>(ws + B.off_slotmat);
-        tb.m = B.m;
-        tb.n = B.n;
-        const char* X = ws + B.off_x[xin];
-        const char* A = ws + B.off_a;
-        const char* Bp = ws + B.off_b;
-        dmuon_status st = DMUON_OK;
-        if (L.kind == DMUON_KIND_GRAM) {
-          st = make_map(&tb.tmA, X, B.n, B.m, B.count, B.x_ld, 64, kTcBM);
-          if (st == DMUON_OK) st = make_map(&tb.tmB, X, B.n, B.m, B.count, B.x_ld, 64, kTcBN);
-          tb.out = ws + B.off_a;
-          tb.out_mat_stride = B.a_mat_bytes;
-          tb.out_ld = B.m_ld;
-          tb.kdim = B.n;
-        } else if (L.kind == DMUON_KIND_POLY) {
-          st = make_map(&tb.tmA, A, B.m, B.m, B.count, B.m_ld, 64, kTcBM);
-          if (st == DMUON_OK) st = make_map(&tb.tmB, A, B.m, B.m, B.count, B.m_ld, 64, kTcBN);
-          tb.out = ws + B.off_b;
-          tb.out_mat_stride = B.a_mat_bytes;
-          tb.out_ld = B.m_ld;
-          tb.aux = A;
-          tb.aux_mat_stride = B.a_mat_bytes;
-          tb.aux_ld = B.m_ld;
-          tb.kdim = B.m;
-        } else {
-          st = make_map(&tb.tmA, Bp, B.m, B.m, B.count, B.m_ld, 64, kTcBM);
-          // X as the MN-major operand: 64 columns (N) x 64 rows (K) per box
-          if (st == DMUON_OK) st = make_map(&tb.tmB, X, B.n, B.m, B.count, B.x_ld, 64, 64);
-          tb.out = last ? nullptr : ws + B.off_x[xout];
-          tb.out_mat_stride = B.x_mat_bytes;
-          tb.out_ld = B.x_ld;
-          tb.aux = X;
-          tb.aux_mat_stride = B.x_mat_bytes;
-          tb.aux_ld = B.x_ld;
-          tb.kdim = B.m;
-        }
+        dmuon_status st = fill_tc_bucket(*P, B, L.phase, L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb]);
         if (st != DMUON_OK) return st;
       }
       tp.items = items + lr.first;
       tp.n_items = lr.count;
-      tp.first = first;
-      tp.last = last;
-      tp.a = a;
-      tp.b = b;
-      tp.c = c;
+      tp.first = L.first;
+      tp.last = L.last;
+      tp.a = L.a;
+      tp.b = L.b;
+      tp.c = L.c;
+      tp.diag = L.diag;
       tp.mats = sp.mats;
       tp.ptrs = sp.ptrs;
       tp.s_norm = sp.s_norm;
@@ -588,68 +845,45 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       L.param_index = static_cast<int>(P->tc_params.size());
       P->tc_params.push_back(tp);
     } else {
-      SimtParams p;
-      std::memset(&p, 0, sizeof(p));
+      SimtParams sm;
+      std::memset(&sm, 0, sizeof(sm));
       for (size_t lb = 0; lb < ch.size(); ++lb) {
         const BucketPlan& B = P->buckets[ch[lb]];
-        SimtBucket& sb = p.bk[lb];
+        SimtBucket& sb = sm.bk[lb];
         sb.slot_mat = reinterpret_cast<const int32_t*>(ws + B.off_slotmat);
         sb.m = B.m;
         sb.n = B.n;
-        const int64_t xs = B.x_mat_bytes / 4, as = B.a_mat_bytes / 4;
-        const float* X = reinterpret_cast<const float*>(ws + B.off_x[xin]);
-        const float* A = reinterpret_cast<const float*>(ws + B.off_a);
-        const float* Bp = reinterpret_cast<const float*>(ws + B.off_b);
-        if (L.kind == DMUON_KIND_GRAM) {
-          sb.opA = sb.opB = X;
-          sb.a_mat_stride = sb.b_mat_stride = xs;
-          sb.a_ld = sb.b_ld = B.x_ld;
-          sb.out = reinterpret_cast<float*>(ws + B.off_a);
-          sb.out_mat_stride = as;
-          sb.out_ld = B.m_ld;
-          sb.kdim = B.n;
-        } else if (L.kind == DMUON_KIND_POLY) {
-          sb.opA = sb.opB = A;
-          sb.a_mat_stride = sb.b_mat_stride = as;
-          sb.a_ld = sb.b_ld = B.m_ld;
-          sb.out = reinterpret_cast<float*>(ws + B.off_b);
-          sb.out_mat_stride = as;
-          sb.out_ld = B.m_ld;
-          sb.aux = A;
-          sb.aux_mat_stride = as;
-          sb.aux_ld = B.m_ld;
-          sb.kdim = B.m;
-        } else {
-          sb.opA = Bp;
-          sb.a_mat_stride = as;
-          sb.a_ld = B.m_ld;
-          sb.opB = X;
-          sb.b_mat_stride = xs;
-          sb.b_ld = B.x_ld;
-          sb.out = last ? nullptr : reinterpret_cast<float*>(ws + B.off_x[xout]);
-          sb.out_mat_stride = xs;
-          sb.out_ld = B.x_ld;
-          sb.aux = X;
-          sb.aux_mat_stride = xs;
-          sb.aux_ld = B.x_ld;
-          sb.kdim = B.m;
-        }
+        const View va = view(B, L.opA), vb = view(B, L.opB), vo = view(B, L.out), vx = view(B, L.aux);
+        sb.opA = reinterpret_cast<const float*>(va.base);
+        sb.a_mat_stride = va.mat_bytes / 4;
+        sb.a_ld = va.ld;
+        sb.opB = reinterpret_cast<const float*>(vb.base);
+        sb.b_mat_stride = vb.mat_bytes / 4;
+        sb.b_ld = vb.ld;
+        sb.out = reinterpret_cast<float*>(vo.base);
+        sb.out_mat_stride = vo.mat_bytes / 4;
+        sb.out_ld = vo.ld;
+        sb.aux = reinterpret_cast<const float*>(vx.base);
+        sb.aux_mat_stride = vx.mat_bytes / 4;
+        sb.aux_ld = vx.ld;
+        sb.kdim = (L.phase == kPhaseGemm) ? B.m : va.inner;
       }
-      p.items = items + lr.first;
-      p.n_items = lr.count;
-      p.first = first;
-      p.last = last;
-      p.a = a;
-      p.b = b;
-      p.c = c;
-      p.mats = sp.mats;
-      p.ptrs = sp.ptrs;
-      p.s_norm = sp.s_norm;
-      p.capture = sp.capture;
-      p.param_bf16 = sp.param_bf16;
+      sm.items = items + lr.first;
+      sm.n_items = lr.count;
+      sm.first = L.first;
+      sm.last = L.last;
+      sm.a = L.a;
+      sm.b = L.b;
+      sm.c = L.c;
+      sm.diag = L.diag;
+      sm.mats = sp.mats;
+      sm.ptrs = sp.ptrs;
+      sm.s_norm = sp.s_norm;
+      sm.capture = sp.capture;
+      sm.param_bf16 = sp.param_bf16;
       L.grid = std::max(1, lr.count);
       L.param_index = static_cast<int>(P->simt_params.size());
-      P->simt_params.push_back(p);
+      P->simt_params.push_back(sm);
     }
   }
 
@@ -718,11 +952,11 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     } else if (P->tc) {
       TcParams& tp = P->tc_params[L.param_index];
       tp.lr = lr;
-      e = launch_tc(L.kind, tp, L.grid, s);
+      e = launch_tc(L.phase, L.bn, tp, L.grid, s);
     } else {
       SimtParams& p = P->simt_params[L.param_index];
       p.lr = lr;
-      e = launch_simt(L.kind, p, L.grid, s);
+      e = launch_simt(L.phase, p, L.grid, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     ++P->launch_count;
@@ -772,8 +1006,11 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
   j += "\"buckets\": [";
   for (size_t b = 0; b < P->buckets.size(); ++b) {
     const BucketPlan& B = P->buckets[b];
-    snprintf(t, sizeof t, "%s{\"m\": %d, \"n\": %d, \"count\": %d, \"transposed\": %d, \"x_ld\": %d, \"m_ld\": %d}",
-             b ? ", " : "", B.m, B.n, B.count, B.n_transposed, B.x_ld, B.m_ld);
+    snprintf(t, sizeof t,
+             "%s{\"m\": %d, \"n\": %d, \"count\": %d, \"transposed\": %d, \"x_ld\": %d, \"m_ld\": %d, "
+             "\"form\": \"%s\", \"bn_sym\": %d, \"bn_gemm\": %d, \"tile_ms\": [%.6g, %.6g, %.6g]}",
+             b ? ", " : "", B.m, B.n, B.count, B.n_transposed, B.x_ld, B.m_ld, B.gram ? "gram" : "standard",
+             B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2]);
     j += t;
   }
   j += "], \"lists\": [";
@@ -785,8 +1022,9 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
   j += "], \"launches\": [";
   for (size_t l = 0; l < P->launches.size(); ++l) {
     const Launch& L = P->launches[l];
-    snprintf(t, sizeof t, "%s{\"kind\": %d, \"step\": %d, \"chunk\": %d, \"grid\": %d, \"work\": %.17g}",
-             l ? ", " : "", L.kind, L.step, L.chunk, L.grid, L.work);
+    snprintf(t, sizeof t,
+             "%s{\"kind\": %d, \"step\": %d, \"chunk\": %d, \"bn\": %d, \"grid\": %d, \"work\": %.17g}",
+             l ? ", " : "", L.kind, L.step, L.chunk, L.bn, L.grid, L.work);
     j += t;
   }
   j += "]}";
@@ -840,6 +1078,30 @@ dmuon_status dmuon_profile_end(dmuon_plan_t P, int32_t* kinds, float* ms, double
     if (work) work[i] = P->prof_work[i];
   }
   destroy_events(*P);
+  return DMUON_OK;
+}
+
+dmuon_status dmuon_plan_costs(dmuon_plan_t P, double* per_matrix_ms, int32_t n) {
+  if (P == nullptr || per_matrix_ms == nullptr) return fail(DMUON_ERR_INVALID_ARG, "NULL argument");
+  if (n != static_cast<int32_t>(P->mats.size())) return fail(DMUON_ERR_INVALID_ARG, "n must equal the plan's n_mats");
+  if (!P->tuned) return fail(DMUON_ERR_UNSUPPORTED, "the plan was not tuned (bind it with DMUON_FLAG_TUNE)");
+  const double S = P->ns_steps;
+  std::vector<int4> t;
+  std::vector<double> per_bucket(P->buckets.size());
+  for (size_t b = 0; b < P->buckets.size(); ++b) {
+    BucketPlan B = P->buckets[b];
+    B.count = 1;
+    t.clear();
+    add_tiles(*P, DMUON_KIND_GRAM, 0, B, t);
+    const double nsym = static_cast<double>(t.size());
+    t.clear();
+    add_tiles(*P, DMUON_KIND_GEMM, 0, B, t);
+    const double ngemm = static_cast<double>(t.size());
+    const double n_xx = B.gram ? 1.0 : S, n_mm = B.gram ? 4.0 * S - 3.0 : S, n_gm = B.gram ? 1.0 : S;
+    // time one SM spends on the matrix, spread over all SMs
+    per_bucket[b] = (nsym * (n_xx * B.tile_ms[0] + n_mm * B.tile_ms[1]) + ngemm * n_gm * B.tile_ms[2]) / P->num_sms;
+  }
+  for (size_t i = 0; i < P->mats.size(); ++i) per_matrix_ms[i] = per_bucket[P->mats[i].bucket];
   return DMUON_OK;
 }
 

@@ -12,12 +12,12 @@ namespace dmuon {
 
 constexpr int kMaxBucketsPerLaunch = 8;
 
-// Tensor-core tile: 128 rows (UMMA M) x 256 columns (UMMA N), K staged 64 at a time.
+// Tensor-core tile: 128 rows (UMMA M) x 256 or 128 columns (UMMA N, chosen per
+// bucket), K staged 64 at a time.
 constexpr int kTcBM = 128;
-constexpr int kTcBN = 256;
+constexpr int kTcBN = 256;  // default tile width
 constexpr int kTcBK = 64;
-constexpr int kTcStages = 4;
-constexpr int kTcThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 epilogue
 
 // fp32 SIMT tile.
 constexpr int kSimtBM = 64;
@@ -89,6 +89,7 @@ struct TcParams {
   int32_t n_items;
   int32_t first, last;
   float a, b, c, lr;
+  float diag;  // poly phase: added on the diagonal (a*I of the Gram-space polynomial)
   const MatDev* mats;
   const uint64_t* ptrs;
   const float* s_norm;
@@ -116,6 +117,7 @@ struct SimtParams {
   int32_t n_items;
   int32_t first, last;
   float a, b, c, lr;
+  float diag;  // poly phase: added on the diagonal
   const MatDev* mats;
   const uint64_t* ptrs;
   const float* s_norm;
@@ -126,10 +128,10 @@ struct SimtParams {
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s);
 cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s);
-cudaError_t launch_tc(int phase, const TcParams& p, int grid, cudaStream_t s);
+int momentum_blocks_per_sm(int grad_bf16, int x_bf16);  // resident CTAs per SM of the momentum kernel
+cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream_t s);
 cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
-size_t tc_smem_bytes();
 
 // Record the message dmuon_last_error() returns on this thread; returns st.
 dmuon_status set_last_error(dmuon_status st, const char* msg);

@@ -41,7 +41,7 @@ __device__ __forceinline__ int find_matrix(const int64_t* unit_begin, int n_mats
 template <bool GB>
 __device__ __forceinline__ void load8_grad(const void* g, int64_t e, float (&x)[8]) {
   if (GB) {
-    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(g) + e);
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(g) + e));
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -50,8 +50,8 @@ __device__ __forceinline__ void load8_grad(const void* g, int64_t e, float (&x)[
       x[2 * k + 1] = f.y;
     }
   } else {
-    const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e);
-    const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e + 4);
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(g) + e + 4));
     x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
   }
 }
@@ -130,68 +130,89 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
       const int64_t total = (int64_t)md.rows * md.cols;
       const int64_t e0 = local * kFlatUnit;
       const int64_t e1 = min(e0 + kFlatUnit, total);
+      constexpr int kV = kFlatUnit / (8 * kStreamThreads);  // 8-element vectors per thread
+      if (e0 + kFlatUnit <= total) {
+        // full unit: every load of the thread is issued before any store
+        float g[kV][8];
+        float4 m0[kV], m1[kV];
 #pragma unroll
-      for (int k = 0; k < kFlatUnit / (8 * kStreamThreads); ++k) {
-        const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
-        if (e + 8 <= e1) {
-          float g[8], uu[8];
-          load8_grad<GB>(G, e, g);
-          float4 m0 = *reinterpret_cast<const float4*>(M + e);
-          float4 m1 = *reinterpret_cast<const float4*>(M + e + 4);
-          float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        for (int k = 0; k < kV; ++k) {
+          const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
+          load8_grad<GB>(G, e, g[k]);
+          m0[k] = __ldcs(reinterpret_cast<const float4*>(M + e));
+          m1[k] = __ldcs(reinterpret_cast<const float4*>(M + e + 4));
+        }
+#pragma unroll
+        for (int k = 0; k < kV; ++k) {
+          const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
+          float mv[8] = {m0[k].x, m0[k].y, m0[k].z, m0[k].w, m1[k].x, m1[k].y, m1[k].z, m1[k].w};
+          float uu[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            mv[q] = fmaf(mu, mv[q], g[q]);
-            uu[q] = nest ? fmaf(mu, mv[q], g[q]) : mv[q];
+            mv[q] = fmaf(mu, mv[q], g[k][q]);
+            uu[q] = nest ? fmaf(mu, mv[q], g[k][q]) : mv[q];
             ss = fmaf(uu[q], uu[q], ss);
           }
-          *reinterpret_cast<float4*>(M + e) = make_float4(mv[0], mv[1], mv[2], mv[3]);
-          *reinterpret_cast<float4*>(M + e + 4) = make_float4(mv[4], mv[5], mv[6], mv[7]);
+          __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
+          __stcs(reinterpret_cast<float4*>(M + e + 4), make_float4(mv[4], mv[5], mv[6], mv[7]));
           store8_x<XB>(X, e, uu);
-        } else {
-          for (int64_t q = e; q < e1 && q < e + 8; ++q) {
-            const float g = load1_grad<GB>(G, q);
-            const float mv = fmaf(mu, M[q], g);
-            const float uu = nest ? fmaf(mu, mv, g) : mv;
-            M[q] = mv;
-            store1_x<XB>(X, q, uu);
-            ss = fmaf(uu, uu, ss);
-          }
+        }
+      } else {
+        for (int64_t q = e0 + threadIdx.x; q < e1; q += kStreamThreads) {
+          const float g = load1_grad<GB>(G, q);
+          const float mv = fmaf(mu, M[q], g);
+          const float uu = nest ? fmaf(mu, mv, g) : mv;
+          M[q] = mv;
+          store1_x<XB>(X, q, uu);
+          ss = fmaf(uu, uu, ss);
         }
       }
     } else {
       const int tr = static_cast<int>(local / md.tiles_c), tc = static_cast<int>(local % md.tiles_c);
       const int r0 = tr * kTileR, c0 = tc * kTileC;
       // read 64 x 128 of G and M (4 consecutive columns per thread), update M, keep U in smem
-#pragma unroll 2
-      for (int pass = 0; pass < kTileR / 8; ++pass) {
-        const int rr = pass * 8 + (threadIdx.x >> 5);
-        const int cc = (threadIdx.x & 31) * 4;
-        const int r = r0 + rr, c = c0 + cc;
-        float uu[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r < md.rows) {
-          const int64_t e = (int64_t)r * md.cols + c;
-          if (md.vec_ok && c + 4 <= md.cols) {
-            float g[4];
-            if (GB) {
-              const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e);
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-              const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-              g[0] = f0.x, g[1] = f0.y, g[2] = f1.x, g[3] = f1.y;
-            } else {
-              const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e);
-              g[0] = f.x, g[1] = f.y, g[2] = f.z, g[3] = f.w;
-            }
-            const float4 m4 = *reinterpret_cast<const float4*>(M + e);
-            float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+      const int cc = (threadIdx.x & 31) * 4;
+      if (md.vec_ok && r0 + kTileR <= md.rows && c0 + kTileC <= md.cols) {
+        // full tile: every load of the thread is issued before any store
+        constexpr int kP = kTileR / 8;
+        float g[kP][4];
+        float4 m4[kP];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              mv[q] = fmaf(mu, mv[q], g[q]);
-              uu[q] = nest ? fmaf(mu, mv[q], g[q]) : mv[q];
-              ss = fmaf(uu[q], uu[q], ss);
-            }
-            *reinterpret_cast<float4*>(M + e) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+        for (int pass = 0; pass < kP; ++pass) {
+          const int rr = pass * 8 + (threadIdx.x >> 5);
+          const int64_t e = (int64_t)(r0 + rr) * md.cols + c0 + cc;
+          if (GB) {
+            const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e));
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
+            g[pass][0] = f0.x, g[pass][1] = f0.y, g[pass][2] = f1.x, g[pass][3] = f1.y;
           } else {
+            const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e));
+            g[pass][0] = f.x, g[pass][1] = f.y, g[pass][2] = f.z, g[pass][3] = f.w;
+          }
+          m4[pass] = __ldcs(reinterpret_cast<const float4*>(M + e));
+        }
+#pragma unroll
+        for (int pass = 0; pass < kP; ++pass) {
+          const int rr = pass * 8 + (threadIdx.x >> 5);
+          const int64_t e = (int64_t)(r0 + rr) * md.cols + c0 + cc;
+          float mv[4] = {m4[pass].x, m4[pass].y, m4[pass].z, m4[pass].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            mv[q] = fmaf(mu, mv[q], g[pass][q]);
+            const float uu = nest ? fmaf(mu, mv[q], g[pass][q]) : mv[q];
+            ss = fmaf(uu, uu, ss);
+            tileU[rr][cc + q] = uu;
+          }
+          __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
+        }
+      } else {
+        for (int pass = 0; pass < kTileR / 8; ++pass) {
+          const int rr = pass * 8 + (threadIdx.x >> 5);
+          const int r = r0 + rr, c = c0 + cc;
+          float uu[4] = {0.f, 0.f, 0.f, 0.f};
+          if (r < md.rows) {
+            const int64_t e = (int64_t)r * md.cols + c;
             for (int q = 0; q < 4 && c + q < md.cols; ++q) {
               const float g = load1_grad<GB>(G, e + q);
               const float mv = fmaf(mu, M[e + q], g);
@@ -200,9 +221,9 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
               ss = fmaf(uu[q], uu[q], ss);
             }
           }
-        }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tileU[rr][cc + q] = uu[q];
+          for (int q = 0; q < 4; ++q) tileU[rr][cc + q] = uu[q];
+        }
       }
       __syncthreads();
       if (md.transposed) {
@@ -308,6 +329,20 @@ __global__ void __launch_bounds__(kStreamThreads) update0_kernel(const __grid_co
 }
 
 }  // namespace
+
+int momentum_blocks_per_sm(int grad_bf16, int x_bf16) {
+  int n = 0;
+  cudaError_t e;
+  if (grad_bf16 && x_bf16)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_kernel<true, true>, kStreamThreads, 0);
+  else if (grad_bf16)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_kernel<true, false>, kStreamThreads, 0);
+  else if (x_bf16)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_kernel<false, true>, kStreamThreads, 0);
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, momentum_kernel<false, false>, kStreamThreads, 0);
+  return (e == cudaSuccess && n > 0) ? n : 1;
+}
 
 cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s) {
   if (p.grad_bf16 && p.x_bf16)

@@ -93,11 +93,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
       float v = acc[r][c];
       if (PHASE == kPhaseGram || PHASE == kPhasePoly) {
         if (j < i) continue;
-        v = (PHASE == kPhaseGram) ? v * sc : p.b * aux[(int64_t)i * B.aux_ld + j] + p.c * v;
+        v = (PHASE == kPhaseGram) ? v * sc
+                                  : p.b * aux[(int64_t)i * B.aux_ld + j] + p.c * v + (i == j ? p.diag : 0.f);
         out[(int64_t)i * B.out_ld + j] = v;
         out[(int64_t)j * B.out_ld + i] = v;
       } else {
-        v = (p.a * aux[(int64_t)i * B.aux_ld + j] + v) * sc;
+        v = ((p.a != 0.f ? p.a * aux[(int64_t)i * B.aux_ld + j] : 0.f) + v) * sc;
         if (!p.last) {
           out[(int64_t)i * B.out_ld + j] = v;
           continue;

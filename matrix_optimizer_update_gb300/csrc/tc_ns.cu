@@ -19,12 +19,20 @@
 // unnormalised U and X0 = s*U with s = 1/(||U||_F + eps), so the gram epilogue
 // multiplies by s^2 and the gemm epilogue by s.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over a cost-ordered
+// The same three kernels also run the Gram-space form of the iteration
+// (gist.science summary section 2, "Gram Space Recurrence"): G = X0 X0^T once,
+// then per step P = a I + b G + c G^2 (poly with a diagonal term),
+// Q <- P Q and G <- (P G) P (symmetric products of commuting symmetric
+// matrices: the gram kernel with two different operands), and finally
+// X = Q X0 (gemm with a = 0) with the W update fused.
+//
+// CTA layout (320 threads, one CTA per SM, persistent over a cost-ordered
 // tile list): warp 0 issues TMA loads of 64-wide K slices into a 4-stage ring
 // of shared-memory buffers (128B swizzle); warp 1 allocates 512 TMEM columns
 // (two 128 x 256 fp32 accumulators) and one thread issues tcgen05.mma
-// (M=128, N=256, K=16); warps 2..5 drain an accumulator with tcgen05.ld while
-// the MMA warp fills the other one. Every wait is bounded (see ptx.cuh).
+// (M=128, N=256, K=16); warps 2..9 drain an accumulator with tcgen05.ld
+// (two warps per TMEM lane quarter, one per column half) while the MMA warp
+// fills the other one. Every wait is bounded (see ptx.cuh).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -36,13 +44,23 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kStageB = kTcBN * kTcBK * 2;  // 32 KB: 256 rows x 128 B (or 4 x [64 k-rows x 128 B])
-constexpr uint32_t kTmemCols = 2 * kTcBN;        // two fp32 accumulators of 256 columns
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
 
+// Tile width N of one CTA (the UMMA N): 256, or 128 for buckets whose edges
+// would leave much of a 256-wide tile empty. Shared-memory stages fill the
+// same ~192 KB either way.
+template <int BN>
+struct TcCfg {
+  static constexpr uint32_t kStageB = BN * kTcBK * 2;  // BN rows x 128 B (or BN/64 x [64 k-rows x 128 B])
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr uint32_t kTmemCols = 2 * BN;        // two fp32 accumulators of BN columns
+  static constexpr int kEpiChunks = BN / 2 / 32;       // 32-column chunks per epilogue warp
+};
+
+template <int STAGES>
 struct TcShared {
-  uint64_t full[kTcStages];
-  uint64_t empty[kTcStages];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -90,20 +108,41 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, int j0, int jmin, int 
   }
 }
 
-// Epilogue of one 32-column chunk of one accumulator row.
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&x)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      x[q * 8 + 2 * e] = f.x;
+      x[q * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// Epilogue of one 32-column chunk of one accumulator row. `pre` holds the
+// chunk's bf16 operand of the linear term (A for poly, X_k for gemm) when the
+// whole chunk lies inside the matrix (fetched before the accumulator was
+// ready); otherwise the operand is read here element by element.
 template <int PHASE>
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket& B, const MatDev& md, int gm,
-                                               int slot, int i, int j0, float sc, float (&v)[32]) {
+                                               int slot, int i, int j0, float sc, float (&v)[32],
+                                               const uint4 (&pre)[4]) {
   if (PHASE == kPhaseGram || PHASE == kPhasePoly) {
     const int m = B.m;
     if (i >= m || j0 >= m || j0 + 31 < i) return;  // nothing of the upper triangle here
     bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride);
     if (PHASE == kPhasePoly) {
-      const bf16* A = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
       float a[32];
-      load_row_bf16(A, j0, m, a);
+      if (j0 + 32 <= m) {
+        unpack_bf16x32(pre, a);
+      } else {
+        const bf16* A = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+        load_row_bf16(A, j0, m, a);
+      }
 #pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = p.b * a[k] + p.c * v[k];
+      for (int k = 0; k < 32; ++k) v[k] = p.b * a[k] + p.c * v[k] + (j0 + k == i ? p.diag : 0.f);
     } else {
 #pragma unroll
       for (int k = 0; k < 32; ++k) v[k] *= sc;
@@ -118,16 +157,25 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
   } else {  // gemm
     const int m = B.m, n = B.n;
     if (i >= m || j0 >= n) return;
-    const bf16* X = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
     float x[32];
-    load_row_bf16(X, j0, n, x);
+    if (p.a == 0.f) {
 #pragma unroll
+      for (int k = 0; k < 32; ++k) x[k] = 0.f;
+    } else if (j0 + 32 <= n) {
+      unpack_bf16x32(pre, x);
+    } else {
+      const bf16* X = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      load_row_bf16(X, j0, n, x);
+    }
+    #pragma unroll
     for (int k = 0; k < 32; ++k) v[k] = (p.a * x[k] + v[k]) * sc;
     if (!p.last) {
       bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride) + (int64_t)i * B.out_ld;
       store_row_bf16(out, j0, 0, n, v);
       return;
     }
+    // W update: every load of the chunk is issued before any store, so the
+    // read-modify-write costs one memory round trip, not 32 dependent ones.
     const float step = p.lr * md.scale;
     void* W = reinterpret_cast<void*>(p.ptrs[gm]);
     if (!md.transposed) {  // W is m x n, row i
@@ -135,10 +183,12 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
         bf16* w = reinterpret_cast<bf16*>(W) + (int64_t)i * n;
         if (j0 + 32 <= n && (n & 7) == 0) {
           uint4* w4 = reinterpret_cast<uint4*>(w + j0);
+          uint4 u[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) u[q] = w4[q];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint4 u = w4[q];
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[q]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               float2 f = __bfloat1622float2(h[e]);
@@ -146,36 +196,47 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
               f.y -= step * v[q * 8 + 2 * e + 1];
               h[e] = __floats2bfloat162_rn(f.x, f.y);
             }
-            w4[q] = u;
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w4[q] = u[q];
         } else {
+          float old[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) old[k] = (j0 + k < n) ? __bfloat162float(w[j0 + k]) : 0.f;
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            if (j0 + k < n) w[j0 + k] = __float2bfloat16_rn(__bfloat162float(w[j0 + k]) - step * v[k]);
+            if (j0 + k < n) w[j0 + k] = __float2bfloat16_rn(old[k] - step * v[k]);
         }
       } else {
         float* w = reinterpret_cast<float*>(W) + (int64_t)i * n;
+        float old[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) old[k] = (j0 + k < n) ? w[j0 + k] : 0.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          if (j0 + k < n) w[j0 + k] -= step * v[k];
+          if (j0 + k < n) w[j0 + k] = old[k] - step * v[k];
       }
-    } else {  // W is n x m: element (j, i); consecutive lanes write consecutive i
-      if (p.param_bf16) {
-        bf16* w = reinterpret_cast<bf16*>(W);
+    } else {  // W is n x m: element (j, i); consecutive lanes touch consecutive i
+      // two halves of 16 columns keep the live addresses and values in registers
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = j0 + k;
-          if (j < n) {
-            bf16* e = w + (int64_t)j * m + i;
-            *e = __float2bfloat16_rn(__bfloat162float(*e) - step * v[k]);
-          }
-        }
-      } else {
-        float* w = reinterpret_cast<float*>(W);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int jh = j0 + hh * 16;
+        if (p.param_bf16) {
+          bf16* w = reinterpret_cast<bf16*>(W) + (int64_t)jh * m + i;
+          float old[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = j0 + k;
-          if (j < n) w[(int64_t)j * m + i] -= step * v[k];
+          for (int k = 0; k < 16; ++k) old[k] = (jh + k < n) ? __bfloat162float(w[k * m]) : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jh + k < n) w[k * m] = __float2bfloat16_rn(old[k] - step * v[hh * 16 + k]);
+        } else {
+          float* w = reinterpret_cast<float*>(W) + (int64_t)jh * m + i;
+          float old[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) old[k] = (jh + k < n) ? w[k * m] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jh + k < n) w[k * m] = old[k] - step * v[hh * 16 + k];
         }
       }
     }
@@ -190,13 +251,18 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
   }
 }
 
-template <int PHASE>
+template <int PHASE, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<BN>;
+  constexpr int kTcStages = C::kStages;
+  constexpr uint32_t kStageB = C::kStageB;
+  constexpr uint32_t kTmemCols = C::kTmemCols;
+  constexpr int kEpiChunks = C::kEpiChunks;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + kTcStages * kStageA;
-  TcShared* sh = reinterpret_cast<TcShared*>(sB + kTcStages * kStageB);
+  TcShared<kTcStages>* sh = reinterpret_cast<TcShared<kTcStages>*>(sB + kTcStages * kStageB);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abortf = &sh->abort_flag;
@@ -244,11 +310,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           ptx::tma_load_3d(sA + stage * kStageA, &B.tmA, &sh->full[stage], k0, it.z * kTcBM, it.y);
           if (PHASE == kPhaseGemm) {
 #pragma unroll
-            for (int q = 0; q < kTcBN / 64; ++q)
+            for (int q = 0; q < BN / 64; ++q)
               ptx::tma_load_3d(sB + stage * kStageB + q * (64 * kTcBK * 2), &B.tmB, &sh->full[stage],
-                               it.w * kTcBN + q * 64, k0, it.y);
+                               it.w * BN + q * 64, k0, it.y);
           } else {
-            ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, it.w * kTcBN, it.y);
+            ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, it.w * BN, it.y);
           }
           ++issued[stage];
           if (++stage == kTcStages) {
@@ -269,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16(kTcBM, kTcBN, PHASE == kPhaseGemm);
+      constexpr uint32_t idesc = ptx::idesc_bf16(kTcBM, BN, PHASE == kPhaseGemm);
       uint32_t stage = 0, phase = 0, local = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
@@ -279,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         const uint32_t acc = local & 1u;
         if (!ptx::mbar_wait(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns)) break;
         ptx::tc_fence_after();
-        const uint32_t d = tmem + acc * kTcBN;
+        const uint32_t d = tmem + acc * BN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(&sh->full[stage], phase, abortf, p.status, p.timeout_ns)) {
             ok = false;
@@ -319,14 +385,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Two warps per TMEM lane quarter (warp % 4), each on one half of the 256 columns.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     uint32_t local = 0;
     for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++local) {
       const uint32_t acc = local & 1u;
-      if (!ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
-      ptx::tc_fence_after();
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
+      const int i = it.z * kTcBM + q * 32 + lane;
+      const int jbase = it.w * BN + half * (BN / 2);
+      // The linear term's operand does not depend on the accumulator: the first
+      // two chunks are fetched while the MMAs of this tile are still running,
+      // each later chunk while the chunk two places before it is processed.
+      const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
+      const bf16* row = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      // gemm with a == 0 (the last product of the Gram-space recurrence) has no linear term
+      const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
+      uint4 cur[4], nxt[4];
+      auto fetch = [&](int ch, uint4 (&dst)[4]) {
+        const int j0 = jbase + ch * 32;
+        if (need_aux && i < B.m && j0 + 32 <= lim) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
+        }
+      };
+      fetch(0, cur);
+      fetch(1, nxt);
+      if (!ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
+      ptx::tc_fence_after();
       const int gm = B.slot_mat[it.y];
       const MatDev md = p.mats[gm];
       float sc = 1.f;
@@ -334,13 +422,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         const float s = p.s_norm[gm];
         sc = (PHASE == kPhaseGram) ? s * s : s;
       }
-      const int i = it.z * kTcBM + q * 32 + lane;
-      const uint32_t tbase = tmem + acc * kTcBN + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int ch = 0; ch < kTcBN / 32; ++ch) {
+      for (int ch = 0; ch < kEpiChunks; ++ch) {
         float v[32];
         ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
-        epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, it.w * kTcBN + ch * 32, sc, v);
+        epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, jbase + ch * 32, sc, v, cur);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+        if (ch + 2 < kEpiChunks) fetch(ch + 2, nxt);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -356,35 +446,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   }
 }
 
-template <int PHASE>
+template <int PHASE, int BN>
+size_t smem_bytes() {
+  using C = TcCfg<BN>;
+  return 1024 + C::kStages * (kStageA + C::kStageB) + sizeof(TcShared<C::kStages>);
+}
+
+template <int PHASE, int BN>
 cudaError_t launch_phase(const TcParams& p, int grid, cudaStream_t s) {
-  static bool configured = false;
-  const size_t smem = tc_smem_bytes();
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_ns_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  tc_ns_kernel<PHASE><<<grid, kTcThreads, smem, s>>>(p);
+  const size_t smem = smem_bytes<PHASE, BN>();
+  cudaError_t e = cudaFuncSetAttribute(tc_ns_kernel<PHASE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  tc_ns_kernel<PHASE, BN><<<grid, kTcThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_bn(int phase, const TcParams& p, int grid, cudaStream_t s) {
+  switch (phase) {
+    case kPhaseGram:
+      return launch_phase<kPhaseGram, BN>(p, grid, s);
+    case kPhasePoly:
+      return launch_phase<kPhasePoly, BN>(p, grid, s);
+    case kPhaseGemm:
+      return launch_phase<kPhaseGemm, BN>(p, grid, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-size_t tc_smem_bytes() { return 1024 + kTcStages * (kStageA + kStageB) + sizeof(TcShared); }
-
-cudaError_t launch_tc(int phase, const TcParams& p, int grid, cudaStream_t s) {
-  switch (phase) {
-    case kPhaseGram:
-      return launch_phase<kPhaseGram>(p, grid, s);
-    case kPhasePoly:
-      return launch_phase<kPhasePoly>(p, grid, s);
-    case kPhaseGemm:
-      return launch_phase<kPhaseGemm>(p, grid, s);
-    default:
-      return cudaErrorInvalidValue;
-  }
+cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream_t s) {
+  if (bn == 256) return launch_bn<256>(phase, p, grid, s);
+  if (bn == 128) return launch_bn<128>(phase, p, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------------ self-test

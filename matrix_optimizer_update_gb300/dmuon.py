@@ -31,19 +31,21 @@ BF16 = 1
 DTYPE = {"f32": F32, "bf16": BF16}
 
 FLAG_CAPTURE_UPDATE = 0x1
+FLAG_GRAM_NS = 0x2
+FLAG_TUNE = 0x4
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 
-KIND_MOMENTUM, KIND_GRAM, KIND_POLY, KIND_GEMM, KIND_UPDATE0 = range(5)
-KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0"}
+KIND_MOMENTUM, KIND_GRAM, KIND_POLY, KIND_GEMM, KIND_UPDATE0, KIND_SYMM = range(6)
+KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0", 5: "symm"}
 
 # every symbol include/dmuon.h declares
 EXPORTS = (
     "dmuon_plan", "dmuon_plan_workspace_bytes", "dmuon_plan_bind", "dmuon_step",
     "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
-    "dmuon_profile_begin", "dmuon_profile_end", "dmuon_launch_count",
-    "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_plan_destroy", "dmuon_last_error",
-    "dmuon_version",
+    "dmuon_profile_begin", "dmuon_profile_end", "dmuon_plan_costs", "dmuon_launch_count",
+    "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_assign_owners", "dmuon_adamw_flat", "dmuon_plan_destroy",
+    "dmuon_last_error", "dmuon_version",
 )
 
 
@@ -87,9 +89,13 @@ def lib():
         "dmuon_profile_begin": (i32, [vp, i32]),
         "dmuon_profile_end": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(f32), ctypes.POINTER(ctypes.c_double),
                                     i32, ctypes.POINTER(i32)]),
+        "dmuon_plan_costs": (i32, [vp, ctypes.POINTER(ctypes.c_double), i32]),
         "dmuon_launch_count": (i32, [vp, ctypes.POINTER(i64)]),
         "dmuon_selftest_wait_timeout": (i32, [vp, i64, vp, ctypes.POINTER(u32)]),
         "dmuon_momentum_norm_noalloc": (i32, [vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, f32, vp]),
+        "dmuon_assign_owners": (i32, [ctypes.POINTER(Shape), i32, i32, ctypes.POINTER(ctypes.c_double), i32,
+                                      ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)]),
+        "dmuon_adamw_flat": (i32, [vp, vp, vp, vp, i64, i32, i32, f32, f32, f32, f32, f32, i32, vp]),
         "dmuon_plan_destroy": (None, [vp]),
         "dmuon_last_error": (ctypes.c_char_p, []),
         "dmuon_version": (i32, []),
@@ -196,6 +202,13 @@ class Plan:
         k = min(n.value, cap)
         return [(kinds[i], ms[i], work[i]) for i in range(k)]
 
+    def costs(self):
+        """Measured per-matrix cost (ms) of a tuned plan."""
+        n = len(self.shapes)
+        out = (ctypes.c_double * n)()
+        _check(lib().dmuon_plan_costs(self._h, out, n))
+        return list(out)
+
     def launch_count(self) -> int:
         c = ctypes.c_int64()
         _check(lib().dmuon_launch_count(self._h, ctypes.byref(c)))
@@ -227,6 +240,27 @@ def dmuon_momentum_norm_noalloc(grad: int, momentum: int, u_out: int, s_out: int
                                              ctypes.c_void_p(s_out), int(rows), int(cols), DTYPE[grad_dtype],
                                              DTYPE[u_dtype], float(mu), int(bool(nesterov)), float(eps),
                                              ctypes.c_void_p(stream)))
+
+
+def dmuon_assign_owners(shapes, n_ranks, ns_steps=5, costs=None):
+    """Owner rank per matrix and the predicted load per rank (host only)."""
+    n = len(shapes)
+    sh = (Shape * max(n, 1))(*[Shape(int(r), int(c)) for r, c in shapes])
+    cs = (ctypes.c_double * n)(*costs) if costs is not None else None
+    own = (ctypes.c_int32 * max(n, 1))()
+    load = (ctypes.c_double * max(n_ranks, 1))()
+    _check(lib().dmuon_assign_owners(sh if n else None, n, ns_steps, cs, n_ranks, own, load))
+    return list(own)[:n], list(load)[:n_ranks]
+
+
+def dmuon_adamw_flat(param: int, grad: int, exp_avg: int, exp_avg_sq: int, n: int, param_dtype="bf16",
+                     grad_dtype="bf16", lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1,
+                     stream: int = 0):
+    """One AdamW step over a flat buffer (see include/dmuon.h)."""
+    _check(lib().dmuon_adamw_flat(ctypes.c_void_p(param), ctypes.c_void_p(grad), ctypes.c_void_p(exp_avg),
+                                  ctypes.c_void_p(exp_avg_sq), int(n), DTYPE[param_dtype], DTYPE[grad_dtype],
+                                  float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step),
+                                  ctypes.c_void_p(stream)))
 
 
 @dataclass

@@ -12,6 +12,7 @@ from .muon_ref import (  # noqa: F401
     momentum_update,
     muon_step,
     newton_schulz,
+    newton_schulz_gram,
     orthogonalize,
     round_to_dtype,
     update_scale,

@@ -97,6 +97,29 @@ def newton_schulz(X: np.ndarray, coeff_steps: Sequence[tuple[float, float, float
     return X
 
 
+def newton_schulz_gram(X: np.ndarray, coeff_steps: Sequence[tuple[float, float, float]]) -> np.ndarray:
+    """The same iteration carried out in the m x m Gram space.
+
+    "DMuon: Efficient Distributed Muon Training with Near-Adam Overhead"
+    (gist.science summary, section 2, "Gram Space Recurrence"): iterate on
+    G = X X^T instead of the m x n matrix when m < n. The pages do not print
+    the recurrence; this is the plain derivation from the quintic step. Each
+    step maps X to P X with P = a I + b G + c G^2 a polynomial in G, so
+    X_k = Q_k X_0 with Q_0 = I, Q_{k+1} = P_k Q_k, and G_{k+1} = P_k G_k P_k.
+    Only the last step touches the m x n matrix again: X_S = Q_S X_0.
+    """
+    X0 = np.asarray(X, dtype=np.float64)
+    m = X0.shape[0]
+    I = np.eye(m)
+    G = X0 @ X0.T
+    Q = I
+    for a, b, c in coeff_steps:
+        P = a * I + b * G + c * (G @ G)
+        Q = P @ Q
+        G = P @ G @ P
+    return Q @ X0
+
+
 def orthogonalize(U: np.ndarray, ns_steps: int, coeffs=DEFAULT_COEFFS, eps: float = 1e-7) -> np.ndarray:
     """Normalise ``U``, run ``ns_steps`` Newton-Schulz steps on the short side,
     and return the result in ``U``'s orientation.

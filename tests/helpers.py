@@ -36,14 +36,17 @@ def storage_ulp(x, dtype):
     return np.ldexp(1.0, (np.floor(np.log2(ax)) - (bits - 1)).astype(int))
 
 
-def weight_rounding_violations(Wg, Wref, Xg, Xref, step, dtype):
+def weight_rounding_violations(Wg, Wref, W0, Xg, Xref, step, dtype):
     """Count elements where the stored weight is not the exact update rounded
-    once to the storage type, up to the update's own error: |Wg - Wref| must
-    not exceed half a storage ulp (at the larger of the two magnitudes) plus
-    step * |Xg - Xref| (+ fp32 slack of the fused subtraction)."""
-    Wg, Wref = np.asarray(Wg, np.float64), np.asarray(Wref, np.float64)
+    once to the storage type, up to the update's own error. The kernel forms
+    y = fl32(W0 - fl32(step * X_gpu)) and rounds y to the storage type, so
+    |Wg - Wref| <= half a storage ulp (at the larger magnitude)
+                   + step * |X_gpu - X_ref|
+                   + (|W0| + step * |X_ref|) * 2^-22   (the fp32 product and difference)."""
+    Wg, Wref, W0 = (np.asarray(a, np.float64) for a in (Wg, Wref, W0))
     big = np.maximum(np.abs(Wg), np.abs(Wref))
-    bound = 0.5 * storage_ulp(big, dtype) + step * np.abs(np.asarray(Xg) - np.asarray(Xref)) + big * 2.0 ** -22 + 1e-30
+    bound = (0.5 * storage_ulp(big, dtype) + step * np.abs(np.asarray(Xg) - np.asarray(Xref))
+             + (np.abs(W0) + step * np.abs(np.asarray(Xref))) * 2.0 ** -22 + 1e-30)
     return int(np.count_nonzero(np.abs(Wg - Wref) > bound))
 
 
@@ -58,7 +61,7 @@ class LibRun:
     """Flat device buffers for one batch plus a bound plan."""
 
     def __init__(self, shapes, *, param="bf16", grad="bf16", compute="bf16", ns_steps=5, coeffs=ref.DEFAULT_COEFFS,
-                 eps=1e-7, capture=True, device="cuda"):
+                 eps=1e-7, capture=True, device="cuda", gram_ns=False):
         self.shapes = list(shapes)
         self.param, self.grad, self.compute = param, grad, compute
         self.offs, total = layout(self.shapes)
@@ -66,7 +69,8 @@ class LibRun:
         self.G = torch.zeros(total, dtype=TORCH_DTYPE[grad], device=device)
         self.M = torch.zeros(total, dtype=torch.float32, device=device)
         self.muon = dm.Muon.create(self.shapes, ns_steps=ns_steps, coeffs=coeffs, eps=eps, param=param, grad=grad,
-                                   compute=compute, flags=dm.FLAG_CAPTURE_UPDATE if capture else 0, device=device)
+                                   compute=compute, device=device,
+                                   flags=(dm.FLAG_CAPTURE_UPDATE if capture else 0) | (dm.FLAG_GRAM_NS if gram_ns else 0))
         self.capture = capture
 
     def view(self, flat, i):
@@ -118,7 +122,7 @@ def compare(run: LibRun, i, W0, G, M0, *, compute, param, lr=0.02, mu=0.95, nest
         Xg = run.update(i).cpu().numpy().astype(np.float64)
         errs["x"] = rel(Xg, Xr)
         r, c = run.shapes[i]
-        errs["w_violations"] = weight_rounding_violations(run.host(run.W, i), Wr, Xg, Xr,
+        errs["w_violations"] = weight_rounding_violations(run.host(run.W, i), Wr, W0, Xg, Xr,
                                                           lr * ref.update_scale(r, c), param)
     errs["m"] = rel(run.host(run.M, i), Mr)
     Wg = run.host(run.W, i)

@@ -75,9 +75,9 @@ def cdiv(a, b):
     return -(-a // b)
 
 
-def brute_tiles(m, n, bm, bn):
-    gram = sum(1 for ti in range(cdiv(m, bm)) for tj in range(cdiv(m, bn)) if tj * bn + bn - 1 >= ti * bm)
-    gemm = cdiv(m, bm) * cdiv(n, bn)
+def brute_tiles(m, n, bm, bn_sym, bn_gemm):
+    gram = sum(1 for ti in range(cdiv(m, bm)) for tj in range(cdiv(m, bn_sym)) if tj * bn_sym + bn_sym - 1 >= ti * bm)
+    gemm = cdiv(m, bm) * cdiv(n, bn_gemm)
     return gram, gemm
 
 
@@ -86,7 +86,7 @@ def test_plan_buckets_tiles_and_work(name):
     w = wl.get(name)
     p = dm.dmuon_plan(w.shapes, w.ns_steps, w.coeffs, w.eps, w.param_dtype, w.grad_dtype, w.compute)
     d = p.describe()
-    bm, bn = d["tile"]
+    bm = d["tile"][0]
     # buckets: one per distinct (short, long) shape, counts and transposed counts add up
     want = {}
     for r, c in w.shapes:
@@ -96,13 +96,21 @@ def test_plan_buckets_tiles_and_work(name):
     got = {(b["m"], b["n"]): (b["count"], b["transposed"]) for b in d["buckets"]}
     assert got == want
     # tile counts: upper-triangle tiles for the symmetric products, full grid for the gemm
-    g_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, bn)[0] for b in d["buckets"])
-    m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, bn)[1] for b in d["buckets"])
+    g_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, b["bn_sym"], b["bn_gemm"])[0] for b in d["buckets"])
+    m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, b["bn_sym"], b["bn_gemm"])[1] for b in d["buckets"])
+    for b in d["buckets"]:
+        if w.compute == "bf16":
+            # 256-wide tiles unless the last one would be at most half full
+            for dim, key in ((b["m"], "bn_sym"), (b["n"], "bn_gemm")):
+                assert b[key] == (128 if 0 < dim % 256 <= 128 else 256), (b, key)
     assert sum(c["gram"] for c in d["lists"]) == g_tot
     assert sum(c["poly"] for c in d["lists"]) == g_tot
     assert sum(c["gemm"] for c in d["lists"]) == m_tot
     # launches per step and the algorithmic work the profiler attributes to them
     assert len(d["launches"]) == 1 + 3 * w.ns_steps * d["chunks"]
+    # every launch of a chunk shares the chunk's tile widths
+    for L in d["launches"][1:]:
+        assert L["bn"] in ((128, 256) if w.compute == "bf16" else (64,))
     work = {}
     for L in d["launches"]:
         work[L["kind"]] = work.get(L["kind"], 0.0) + L["work"]
@@ -133,3 +141,34 @@ def test_plan_is_deterministic():
     a = dm.dmuon_plan(w.shapes, 5).describe()
     b = dm.dmuon_plan(w.shapes, 5).describe()
     assert a == b
+
+
+def test_gram_form_plan_launches_and_work():
+    w = wl.get("llama-3.1-8b")
+    S = w.ns_steps
+    p = dm.dmuon_plan(w.shapes, S, flags=dm.FLAG_GRAM_NS)
+    d = p.describe()
+    forms = {(b["m"], b["n"]): b["form"] for b in d["buckets"]}
+    assert forms == {(4096, 14336): "gram", (4096, 4096): "standard", (1024, 4096): "gram"}
+    std_chunks, gram_chunks = 1, 1
+    assert len(d["launches"]) == 1 + 3 * S * std_chunks + (4 * S - 1) * gram_chunks
+    # executed work: standard buckets as before; Gram buckets: X X^T once, S polys, (S-1) Q products,
+    # 2(S-1) G products (symmetric products counted once) and the final 2 m^2 n product
+    want = 0.0
+    for r, c in w.shapes:
+        m, n = min(r, c), max(r, c)
+        if n > m:
+            sym = m * m * (m + 1)
+            want += m * (m + 1) * n + S * sym + (S - 1) * sym + 2 * (S - 1) * sym + 2 * m * m * n
+        else:
+            want += wl.ns_flops(r, c, S)
+    got = sum(L["work"] for L in d["launches"] if L["kind"] != dm.KIND_MOMENTUM)
+    assert abs(got - want) / want < 1e-12
+    assert got < 0.6 * sum(wl.ns_flops(r, c, S) for r, c in w.shapes)
+
+
+def test_costs_need_a_tuned_plan():
+    p = dm.dmuon_plan([(64, 128)], 5, flags=dm.FLAG_TUNE)
+    with pytest.raises(dm.DmuonError) as e:
+        p.costs()
+    assert e.value.status == dm.ERR_UNSUPPORTED

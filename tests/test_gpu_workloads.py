@@ -42,15 +42,17 @@ def sample_indices(w):
     return [i for i, m in enumerate(mats) if m[0] in (0, L - 1)]
 
 
-@pytest.mark.parametrize("name", ["qwen2.5-1.5b", "llama-3.2-3b", "llama-3.1-8b", "moe-16x64"])
-def test_workload_parity(name):
+@pytest.mark.parametrize("name,gram", [("qwen2.5-1.5b", False), ("llama-3.2-3b", False), ("llama-3.1-8b", False),
+                                       ("moe-16x64", False), ("llama-3.1-8b", True), ("moe-16x64", True)])
+def test_workload_parity(name, gram):
     w = wl.get(name)
     ms = make_matrix_set(w, "cuda")
     idx = sample_indices(w)
     before = {i: (ms.view(ms.W, i).double().cpu().numpy(), ms.view(ms.G, i).double().cpu().numpy(),
                   ms.view(ms.M, i).double().cpu().numpy()) for i in idx}
     muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
-                          grad=w.grad_dtype, compute=w.compute, flags=dm.FLAG_CAPTURE_UPDATE)
+                          grad=w.grad_dtype, compute=w.compute,
+                          flags=dm.FLAG_CAPTURE_UPDATE | (dm.FLAG_GRAM_NS if gram else 0))
     stream = torch.cuda.current_stream().cuda_stream
     muon.plan.step(ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M), w.lr, w.mu, w.nesterov, stream)
     torch.cuda.synchronize()
@@ -58,9 +60,9 @@ def test_workload_parity(name):
 
     # properties of every matrix: finite weights, and ||X||_F / sqrt(m) inside the band
     # [0.68, 1.21] that the quintic maps every normalised singular value >= 3e-3 into
-    assert bool(torch.isfinite(ms.W.float()).all())
     x = torch.empty(max(r * c for r, c in w.shapes), dtype=torch.float32, device="cuda")
     for i, (r, c) in enumerate(w.shapes):
+        assert bool(torch.isfinite(ms.view(ms.W, i)).all()), i
         muon.plan.read_update(i, x.data_ptr(), stream)
         nrm = float(torch.linalg.vector_norm(x[: r * c])) / np.sqrt(min(r, c))
         assert 0.68 <= nrm <= 1.21, (i, r, c, nrm)
@@ -82,5 +84,5 @@ def test_workload_parity(name):
         assert ex <= TOL_X[w.compute], (i, r, c, ex)
         assert ew <= TOL_W[w.param_dtype], (i, r, c, ew)
         assert em <= TOL_M, (i, r, c, em)
-        assert weight_rounding_violations(Wg, Wr, Xg, Xr, w.lr * ref.update_scale(r, c), w.param_dtype) == 0
-    print(name, "sampled", len(idx), "worst", worst)
+        assert weight_rounding_violations(Wg, Wr, W0, Xg, Xr, w.lr * ref.update_scale(r, c), w.param_dtype) == 0
+    print(name, "gram" if gram else "standard", "sampled", len(idx), "worst", worst)

@@ -215,3 +215,17 @@ def test_golden_tiny_step_regression():
         # and the stored X is itself the scalar map of the normalised singular values
         np.testing.assert_allclose(np.array(case["X"]), spectral_expected(G + h["mu"] * (h["mu"] * M + G), h["ns_steps"]),
                                    rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("shape", [(4, 9), (16, 40), (32, 112), (5, 5), (1, 8)])
+def test_gram_space_recurrence_equals_the_iteration(shape):
+    # X_S = Q_S X_0 with Q, G polynomials in X_0 X_0^T: the identity holds exactly in exact arithmetic
+    for seed in range(5):
+        U = np.random.default_rng(seed).standard_normal(shape)
+        X0 = U / np.linalg.norm(U)
+        steps = [ref.DEFAULT_COEFFS] * 5
+        np.testing.assert_allclose(ref.newton_schulz_gram(X0, steps), ref.newton_schulz(X0, steps), rtol=0,
+                                   atol=1e-11)
+        # and against the scalar map of the singular values
+        np.testing.assert_allclose(ref.newton_schulz_gram(X0, steps), spectral_expected(U, 5, eps=0.0), rtol=0,
+                                   atol=1e-10)
