@@ -301,7 +301,16 @@ def run_ours(args):
     ns_kinds = {k: v for k, v in per_kind.items() if k in NS_KINDS}
     dom = max(ns_kinds, key=lambda k: ns_kinds[k]["ms"]) if ns_kinds else max(per_kind, key=lambda k: per_kind[k]["ms"])
     d = per_kind[dom]
-    if dom in NS_KINDS:
+    if dom in NS_KINDS and w.compute == "f32":
+        # fp32 mode runs on the CUDA cores: FFMA peak = SMs x 128 lanes x 2 flops x max SM clock
+        props = torch.cuda.get_device_properties(local)
+        alu_peak = props.multi_processor_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "peak_source": "SMs x 128 FP32 lanes x 2 x max SM clock",
+                "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
+                "traffic": None}
+    elif dom in NS_KINDS:
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved / tensor_peak, "peak_source": f"{peak_src} bf16_tflops_sustained",

@@ -81,7 +81,7 @@ typedef struct {
 /* Plan flags. */
 #define DMUON_FLAG_CAPTURE_UPDATE 0x1u /* keep the fp32 update X of the last step
                                           (read it with dmuon_read_update)      */
-#define DMUON_FLAG_GRAM_NS 0x2u        /* matrices with max(rows,cols) > min(rows,cols)
+#define DMUON_FLAG_GRAM_NS 0x2u        /* matrices with max(rows,cols) >= 2*min(rows,cols)
                                           iterate in the m x m Gram space: G = X X^T
                                           once, then per step P = aI + bG + cG^2,
                                           Q <- P Q, G <- P G P; finally X = Q X0
@@ -89,8 +89,8 @@ typedef struct {
                                           Training with Near-Adam Overhead",
                                           gist.science summary section 2, "Gram
                                           Space Recurrence"). Fewer flops when the
-                                          matrix is wide; square ones keep the
-                                          standard form.                         */
+                                          matrix is wide (>= 26% fewer at 2:1);
+                                          others keep the standard form.          */
 #define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
                                           per bucket on the bound workspace, keep
                                           the faster, and order tiles by measured

@@ -231,7 +231,8 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].n = order[b].second;
     P.buckets[b].x_ld = static_cast<int32_t>(align_up(order[b].second, ld_mult));
     P.buckets[b].m_ld = static_cast<int32_t>(align_up(order[b].first, ld_mult));
-    P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second > order[b].first;
+    // the Gram-space form pays (>= 26% fewer flops) and keeps bf16 accuracy on wide matrices only
+    P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn(order[b].second) : kSimtBN;
   }

@@ -157,7 +157,7 @@ def test_gram_form_plan_launches_and_work():
     want = 0.0
     for r, c in w.shapes:
         m, n = min(r, c), max(r, c)
-        if n > m:
+        if n >= 2 * m:
             sym = m * m * (m + 1)
             want += m * (m + 1) * n + S * sym + (S - 1) * sym + 2 * (S - 1) * sym + 2 * m * m * n
         else:

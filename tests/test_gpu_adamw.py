@@ -48,9 +48,16 @@ def test_adamw_matches_oracle(pdt, gdt, n):
         assert np.all(np.abs(mg - mr) <= 2.0 ** -21 * m_terms + 1e-30)
         assert np.all(np.abs(vg - vr) <= 2.0 ** -21 * v_terms + 1e-30)
         pg = p.double().cpu().numpy()
-        # stored parameter = exact step rounded once to its storage type (+ fp32 arithmetic slack)
-        bound = 0.5 * storage_ulp(np.maximum(np.abs(pg), np.abs(pr)), pdt) + 1e-5 * np.abs(pr - p_before) + \
-            np.abs(p_before) * 2.0 ** -21
+        # stored parameter = exact step rounded once to its storage type, up to the fp32 arithmetic:
+        # the moments' own error (bounded above) carried through m / (sqrt(v)/sqrt(bc2) + eps), plus a
+        # few ulps of the decay and of the update
+        bc1, bc2 = 1 - f(0.9) ** step, 1 - f(0.999) ** step
+        den = np.sqrt(vr) / np.sqrt(bc2) + f(1e-8)
+        upd = f(1e-3) / bc1 * mr / den
+        dm_max, dv_max = 2.0 ** -21 * m_terms, 2.0 ** -21 * v_terms
+        dden = dv_max / (2 * np.sqrt(np.maximum(vr, 1e-300)) * np.sqrt(bc2))
+        dupd = f(1e-3) / bc1 * (dm_max / den + np.abs(mr) * dden / den ** 2) + np.abs(upd) * 2.0 ** -20
+        bound = 0.5 * storage_ulp(np.maximum(np.abs(pg), np.abs(pr)), pdt) + np.abs(p_before) * 2.0 ** -21 + dupd
         assert int(np.count_nonzero(np.abs(pg - pr) > bound)) == 0
         mr, vr = mg, vg  # continue from the stored moments
 

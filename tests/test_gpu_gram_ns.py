@@ -16,7 +16,7 @@ def test_gram_form_ragged_shapes(compute):
     prm = "bf16" if compute == "bf16" else "f32"
     run = LibRun(RAGGED, param=prm, grad=prm, compute=compute, gram_ns=True)
     forms = {(b["m"], b["n"]): b["form"] for b in run.muon.plan.describe()["buckets"]}
-    assert forms[(130, 130)] == "standard" and forms[(300, 700)] == "gram"
+    assert forms[(130, 130)] == "standard" and forms[(300, 700)] == "gram" and forms[(129, 257)] == "standard"
     init = _fill(run, 700, grad_std=1e-3 if compute == "bf16" else 1.0, w_std=0.02 if compute == "bf16" else 1.0,
                  m_std=1e-3)
     run.step()
