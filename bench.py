@@ -241,8 +241,10 @@ def run_ours(args):
     tot = wl.totals(w)
     ms = make_matrix_set(w, f"cuda:{local}", seed_offset=replica_seed_offset(rank))
     stream = torch.cuda.Stream()
+    tile_flags = dm.FLAG_PAIR_TILES if args.pair else 0
     muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
-                          grad=w.grad_dtype, compute=w.compute, device=f"cuda:{local}", stream=stream)
+                          grad=w.grad_dtype, compute=w.compute, flags=tile_flags, device=f"cuda:{local}",
+                          stream=stream)
     plan = muon.plan
     desc = plan.describe()
     launches_per_step = len(desc["launches"])
@@ -336,7 +338,8 @@ def run_ours(args):
     gram = None
     if not args.no_gram and w.compute == "bf16":
         gm = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
-                            grad=w.grad_dtype, compute=w.compute, flags=dm.FLAG_GRAM_NS, device=f"cuda:{local}",
+                            grad=w.grad_dtype, compute=w.compute, flags=dm.FLAG_GRAM_NS | tile_flags,
+                            device=f"cuda:{local}",
                             stream=stream)
         gplan = gm.plan
         glps = len(gplan.describe()["launches"])
@@ -445,7 +448,7 @@ def run_ours(args):
         "config": {"workload": w.name, "matrices": tot["matrices"], "params": tot["params"],
                    "ns_steps": w.ns_steps, "ns_flops_per_step": tot["ns_flops"],
                    "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
-                   "parallelism": f"replicas{world}",
+                   "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
         "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
@@ -474,6 +477,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
+    ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
     if args.impl == "reference":

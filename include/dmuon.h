@@ -91,6 +91,11 @@ typedef struct {
                                           Space Recurrence"). Fewer flops when the
                                           matrix is wide (>= 26% fewer at 2:1);
                                           others keep the standard form.          */
+#define DMUON_FLAG_PAIR_TILES 0x8u    /* buckets whose short side is >= 256 and
+                                          whose products run 256 wide use
+                                          256 x 256 tiles on pairs of SMs
+                                          (two-SM UMMA, thread-block clusters of
+                                          2). bf16 only.                        */
 #define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
                                           per bucket on the bound workspace, keep
                                           the faster, and order tiles by measured

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdmuon.so")
-SOURCES = ["api.cu", "momentum.cu", "tc_ns.cu", "simt_ns.cu", "noalloc.cu", "owners.cpp", "adamw.cu"]
+SOURCES = ["api.cu", "momentum.cu", "tc_ns.cu", "tc_ns2.cu", "simt_ns.cu", "noalloc.cu", "owners.cpp", "adamw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -62,6 +62,7 @@ struct BucketPlan {
   int32_t m = 0, n = 0, count = 0, n_transposed = 0;
   int32_t x_ld = 0, m_ld = 0;
   bool gram = false;          // iterate in the m x m Gram space
+  bool pair = false;          // 256 x 256 tiles on CTA pairs (two-SM UMMA)
   int32_t bn_sym = 0;         // tile width of the symmetric products (m x m outputs)
   int32_t bn_gemm = 0;        // tile width of the m x n product
   double tile_ms[3] = {0, 0, 0};  // measured ms per tile: X X^T (K = n), m x m products, gemm; 0 = not measured
@@ -86,6 +87,7 @@ struct Launch {
   int chunk = 0;
   int list = 0;   // ListKind
   int bn = 0;     // tile width of this launch
+  bool pair = false;  // two-SM tiles
   int opA = kBufNone, opB = kBufNone, out = kBufNone, aux = kBufNone;
   float a = 0.f, b = 0.f, c = 0.f, diag = 0.f;
   int first = 0, last = 0;
@@ -183,7 +185,7 @@ int32_t default_bn(int d) {
 
 // Tiles of one phase for one bucket, appended in cost order.
 void add_tiles(const dmuon_plan_s& P, int kind, int bucket_local, const BucketPlan& B, std::vector<int4>& out) {
-  const int BM = P.tile_m, BN = (kind == DMUON_KIND_GEMM) ? B.bn_gemm : B.bn_sym;
+  const int BM = B.pair ? 256 : P.tile_m, BN = (kind == DMUON_KIND_GEMM) ? B.bn_gemm : B.bn_sym;
   const int tm = static_cast<int>(cdiv(B.m, BM));
   if (kind == DMUON_KIND_GEMM) {
     const int tn = static_cast<int>(cdiv(B.n, BN));
@@ -235,6 +237,9 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn(order[b].second) : kSimtBN;
+    // two-SM 256 x 256 tiles where both dimensions fill them
+    P.buckets[b].pair = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES) && order[b].first >= 256 &&
+                        P.buckets[b].bn_sym == 256 && P.buckets[b].bn_gemm == 256;
   }
 
   P.mats.assign(n_mats, MatDev{});
@@ -287,9 +292,9 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   P.chunks.clear();
   P.chunk_gram.clear();
   {
-    std::vector<std::tuple<int, int, int>> keys;
+    std::vector<std::tuple<int, int, int, int>> keys;
     for (const BucketPlan& B : P.buckets) {
-      const auto k = std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm);
+      const auto k = std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm, (int)B.pair);
       if (std::find(keys.begin(), keys.end(), k) == keys.end()) keys.push_back(k);
     }
     std::stable_sort(keys.begin(), keys.end(),
@@ -298,7 +303,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
       std::vector<int> ch;
       for (size_t b = 0; b < P.buckets.size(); ++b) {
         const BucketPlan& B = P.buckets[b];
-        if (std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm) != k) continue;
+        if (std::make_tuple((int)B.gram, B.bn_sym, B.bn_gemm, (int)B.pair) != k) continue;
         ch.push_back(static_cast<int>(b));
         if (ch.size() == kMaxBucketsPerLaunch) {
           P.chunks.push_back(ch);
@@ -424,6 +429,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
     x.chunk = chunk;
     x.list = list;
     x.bn = (phase == kPhaseGemm) ? P.buckets[P.chunks[chunk][0]].bn_gemm : P.buckets[P.chunks[chunk][0]].bn_sym;
+    x.pair = P.buckets[P.chunks[chunk][0]].pair;
     x.opA = opA;
     x.opB = opB;
     x.out = out;
@@ -589,6 +595,7 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
     for (int bi = 0; bi < 2 && st == DMUON_OK; ++bi) {
       BucketPlan T = B;
       T.bn_sym = T.bn_gemm = bns[bi];
+      T.pair = false;  // the probes time one-SM tiles
       for (int kind = 0; kind < 3 && st == DMUON_OK; ++kind) {
         tiles.clear();
         add_tiles(P, kind == 2 ? DMUON_KIND_GEMM : DMUON_KIND_GRAM, 0, T, tiles);
@@ -651,6 +658,7 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
     }
     B.bn_sym = bns[bs];
     B.bn_gemm = bns[bg];
+    if (B.pair && (B.bn_sym != 256 || B.bn_gemm != 256)) B.pair = false;  // pairs run 256-wide tiles only
     B.tile_ms[0] = tms[bs][0];
     B.tile_ms[1] = tms[bs][1];
     B.tile_ms[2] = tms[bg][2];
@@ -685,7 +693,7 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (shapes == nullptr || n_mats <= 0) return fail(DMUON_ERR_INVALID_ARG, "empty matrix list");
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
-  if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE))
+  if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES))
     return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
@@ -824,7 +832,8 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       std::memset(&tp, 0, sizeof(tp));
       for (size_t lb = 0; lb < ch.size(); ++lb) {
         const BucketPlan& B = P->buckets[ch[lb]];
-        dmuon_status st = fill_tc_bucket(*P, B, L.phase, L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb]);
+        // a pair's CTAs each load 128 rows of a K-major B operand
+        dmuon_status st = fill_tc_bucket(*P, B, L.phase, L.pair ? 128 : L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb]);
         if (st != DMUON_OK) return st;
       }
       tp.items = items + lr.first;
@@ -842,7 +851,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       tp.status = sp.status;
       tp.param_bf16 = sp.param_bf16;
       tp.timeout_ns = 2000000000LL;
-      L.grid = std::max(1, std::min(lr.count, P->num_sms));
+      L.grid = L.pair ? std::max(1, std::min(lr.count, P->num_sms / 2)) : std::max(1, std::min(lr.count, P->num_sms));
       L.param_index = static_cast<int>(P->tc_params.size());
       P->tc_params.push_back(tp);
     } else {
@@ -953,7 +962,7 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     } else if (P->tc) {
       TcParams& tp = P->tc_params[L.param_index];
       tp.lr = lr;
-      e = launch_tc(L.phase, L.bn, tp, L.grid, s);
+      e = L.pair ? launch_tc_pair(L.phase, tp, L.grid, s) : launch_tc(L.phase, L.bn, tp, L.grid, s);
     } else {
       SimtParams& p = P->simt_params[L.param_index];
       p.lr = lr;
@@ -1009,9 +1018,10 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
     const BucketPlan& B = P->buckets[b];
     snprintf(t, sizeof t,
              "%s{\"m\": %d, \"n\": %d, \"count\": %d, \"transposed\": %d, \"x_ld\": %d, \"m_ld\": %d, "
-             "\"form\": \"%s\", \"bn_sym\": %d, \"bn_gemm\": %d, \"tile_ms\": [%.6g, %.6g, %.6g]}",
+             "\"form\": \"%s\", \"pair\": %s, \"bn_sym\": %d, \"bn_gemm\": %d, "
+             "\"tile_ms\": [%.6g, %.6g, %.6g]}",
              b ? ", " : "", B.m, B.n, B.count, B.n_transposed, B.x_ld, B.m_ld, B.gram ? "gram" : "standard",
-             B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2]);
+             B.pair ? "true" : "false", B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2]);
     j += t;
   }
   j += "], \"lists\": [";
@@ -1024,8 +1034,9 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
   for (size_t l = 0; l < P->launches.size(); ++l) {
     const Launch& L = P->launches[l];
     snprintf(t, sizeof t,
-             "%s{\"kind\": %d, \"step\": %d, \"chunk\": %d, \"bn\": %d, \"grid\": %d, \"work\": %.17g}",
-             l ? ", " : "", L.kind, L.step, L.chunk, L.bn, L.grid, L.work);
+             "%s{\"kind\": %d, \"step\": %d, \"chunk\": %d, \"bn\": %d, \"pair\": %s, \"grid\": %d, "
+             "\"work\": %.17g}",
+             l ? ", " : "", L.kind, L.step, L.chunk, L.bn, L.pair ? "true" : "false", L.grid, L.work);
     j += t;
   }
   j += "]}";

@@ -130,6 +130,8 @@ cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s);
 cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s);
 int momentum_blocks_per_sm(int grad_bf16, int x_bf16);  // resident CTAs per SM of the momentum kernel
 cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream_t s);
+// Two-SM form: 256 x 256 tiles on clusters of two CTAs; `pairs` clusters.
+cudaError_t launch_tc_pair(int phase, const TcParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
 

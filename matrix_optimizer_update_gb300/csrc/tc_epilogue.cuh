@@ -1,0 +1,200 @@
+// tc_epilogue.cuh - epilogue of the Newton-Schulz tensor-core kernels: one
+// 32-column chunk of one accumulator row (fp32, read from TMEM) turned into
+// the phase's output (symmetric store with mirror, polynomial term, a*X term,
+// or the fused weight update).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace dmuon {
+namespace epi {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ void load_row_bf16(const bf16* src, int j0, int lim, float (&x)[32]) {
+  if (j0 + 32 <= lim) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + j0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u = s4[q];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(h[e]);
+        x[q * 8 + 2 * e] = f.x;
+        x[q * 8 + 2 * e + 1] = f.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[k] = (j0 + k < lim) ? __bfloat162float(src[j0 + k]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_row_bf16(bf16* dst, int j0, int jmin, int lim, const float (&v)[32]) {
+  if (j0 >= jmin && j0 + 32 <= lim) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst + j0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+      d4[q] = u;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int j = j0 + k;
+      if (j >= jmin && j < lim) dst[j] = __float2bfloat16_rn(v[k]);
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&x)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      x[q * 8 + 2 * e] = f.x;
+      x[q * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// Epilogue of one 32-column chunk of one accumulator row. `pre` holds the
+// chunk's bf16 operand of the linear term (A for poly, X_k for gemm) when the
+// whole chunk lies inside the matrix (fetched before the accumulator was
+// ready); otherwise the operand is read here element by element.
+template <int PHASE>
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket& B, const MatDev& md, int gm,
+                                               int slot, int i, int j0, float sc, float (&v)[32],
+                                               const uint4 (&pre)[4]) {
+  if (PHASE == kPhaseGram || PHASE == kPhasePoly) {
+    const int m = B.m;
+    if (i >= m || j0 >= m || j0 + 31 < i) return;  // nothing of the upper triangle here
+    bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride);
+    if (PHASE == kPhasePoly) {
+      float a[32];
+      if (j0 + 32 <= m) {
+        unpack_bf16x32(pre, a);
+      } else {
+        const bf16* A = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+        load_row_bf16(A, j0, m, a);
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = p.b * a[k] + p.c * v[k] + (j0 + k == i ? p.diag : 0.f);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] *= sc;
+    }
+    // own row: columns j >= i; mirror: (j, i) for j > i (coalesced across the warp's 32 rows)
+    store_row_bf16(out + (int64_t)i * B.out_ld, j0, i, m, v);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int j = j0 + k;
+      if (j > i && j < m) out[(int64_t)j * B.out_ld + i] = __float2bfloat16_rn(v[k]);
+    }
+  } else {  // gemm
+    const int m = B.m, n = B.n;
+    if (i >= m || j0 >= n) return;
+    float x[32];
+    if (p.a == 0.f) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) x[k] = 0.f;
+    } else if (j0 + 32 <= n) {
+      unpack_bf16x32(pre, x);
+    } else {
+      const bf16* X = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      load_row_bf16(X, j0, n, x);
+    }
+    #pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = (p.a * x[k] + v[k]) * sc;
+    if (!p.last) {
+      bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride) + (int64_t)i * B.out_ld;
+      store_row_bf16(out, j0, 0, n, v);
+      return;
+    }
+    // W update: every load of the chunk is issued before any store, so the
+    // read-modify-write costs one memory round trip, not 32 dependent ones.
+    const float step = p.lr * md.scale;
+    void* W = reinterpret_cast<void*>(p.ptrs[gm]);
+    if (!md.transposed) {  // W is m x n, row i
+      if (p.param_bf16) {
+        bf16* w = reinterpret_cast<bf16*>(W) + (int64_t)i * n;
+        if (j0 + 32 <= n && (n & 7) == 0) {
+          uint4* w4 = reinterpret_cast<uint4*>(w + j0);
+          uint4 u[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) u[q] = w4[q];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[q]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float2 f = __bfloat1622float2(h[e]);
+              f.x -= step * v[q * 8 + 2 * e];
+              f.y -= step * v[q * 8 + 2 * e + 1];
+              h[e] = __floats2bfloat162_rn(f.x, f.y);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w4[q] = u[q];
+        } else {
+          float old[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) old[k] = (j0 + k < n) ? __bfloat162float(w[j0 + k]) : 0.f;
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (j0 + k < n) w[j0 + k] = __float2bfloat16_rn(old[k] - step * v[k]);
+        }
+      } else {
+        float* w = reinterpret_cast<float*>(W) + (int64_t)i * n;
+        float old[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) old[k] = (j0 + k < n) ? w[j0 + k] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (j0 + k < n) w[j0 + k] = old[k] - step * v[k];
+      }
+    } else {  // W is n x m: element (j, i); consecutive lanes touch consecutive i
+      // two halves of 16 columns keep the live addresses and values in registers
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int jh = j0 + hh * 16;
+        if (p.param_bf16) {
+          bf16* w = reinterpret_cast<bf16*>(W) + (int64_t)jh * m + i;
+          float old[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) old[k] = (jh + k < n) ? __bfloat162float(w[k * m]) : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jh + k < n) w[k * m] = __float2bfloat16_rn(old[k] - step * v[hh * 16 + k]);
+        } else {
+          float* w = reinterpret_cast<float*>(W) + (int64_t)jh * m + i;
+          float old[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) old[k] = (jh + k < n) ? w[k * m] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jh + k < n) w[k * m] = old[k] - step * v[hh * 16 + k];
+        }
+      }
+    }
+    if (p.capture != nullptr && md.cap_off >= 0) {
+      float* cap = p.capture + md.cap_off;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        if (j < n) cap[md.transposed ? (int64_t)j * m + i : (int64_t)i * n + j] = v[k];
+      }
+    }
+  }
+}
+
+}  // namespace epi
+}  // namespace dmuon

@@ -1,0 +1,280 @@
+// tc_ns2.cu - the Newton-Schulz products on CTA pairs: two-SM UMMA
+// (tcgen05 cta_group::2), 256 x 256 output tiles.
+//
+// Same phases and epilogues as tc_ns.cu (gram / poly / gemm, see there). A
+// cluster of two CTAs on neighbouring SMs owns one tile: each CTA loads its
+// 128 rows of A and one half (128 rows, or 128 columns for the MN-major X
+// operand of the gemm) of B into its own shared memory, the leader CTA
+// (cluster rank 0) issues tcgen05.mma.cta_group::2 with M = 256, N = 256,
+// and the 256 x 256 fp32 accumulator lands half in each CTA's TMEM. Per SM
+// that moves 32 KB of operands per 4.2 MFLOP instead of 48 KB with one-SM
+// 128 x 256 tiles.
+//
+// Synchronisation across the pair:
+//  - full[s] lives in the leader; both CTAs' TMA loads count their bytes on
+//    it (.cta_group::2 lets a load signal the peer's barrier), the leader
+//    alone sets the expected byte count;
+//  - empty[s] and tfull[a] live in both CTAs; the leader's commits arrive
+//    on both (multicast::cluster);
+//  - tempty[a] lives in the leader and collects one arrival per epilogue
+//    warp of both CTAs;
+//  - cluster barriers after set-up and before TMEM is released, so that no
+//    CTA signals an uninitialised barrier or leaves while the leader's MMAs
+//    still read its shared memory or write its TMEM.
+// All mbarrier waits are bounded as in tc_ns.cu.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_epilogue.cuh"
+
+namespace dmuon {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kPairBM = 256;                   // rows of a pair tile (128 per CTA)
+constexpr int kPairBN = 256;                   // columns of a pair tile
+constexpr uint32_t kHalfA = 128 * kTcBK * 2;   // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t kHalfB = 128 * kTcBK * 2;   // 16 KB: this CTA's half of B
+constexpr int kStages = 6;
+constexpr uint32_t kTmemCols = 2 * kPairBN;    // two 128 x 256 fp32 accumulators per CTA
+constexpr int kEpiWarps = 8;
+constexpr int kEpiChunks = kPairBN / 2 / 32;
+
+struct PairShared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int PHASE>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kStages * kHalfA;
+  PairShared* sh = reinterpret_cast<PairShared*>(sB + kStages * kHalfB);
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abortf = &sh->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&sh->full[s], 1);
+      ptx::mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&sh->tfull[a], 1);
+      ptx::mbar_init(&sh->tempty[a], 2 * kEpiWarps);
+    }
+    ptx::mbar_init(&sh->mma_done, 1);
+    sh->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(&sh->tmem_base, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      const uint32_t lead_full = ptx::mapa_shared(ptx::smem_u32(&sh->full[0]), 0);
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      for (int w = pair; w < p.n_items; w += npairs) {
+        const int4 it = p.items[w];
+        const TcBucket& B = p.bk[it.x];
+        const int nk = (B.kdim + kTcBK - 1) / kTcBK;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(&sh->empty[stage], phase ^ 1u, abortf, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          if (leader) ptx::mbar_arrive_expect_tx(&sh->full[stage], 2 * (kHalfA + kHalfB));
+          const uint32_t fb = lead_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
+          const int k0 = kb * kTcBK;
+          ptx::tma_load_3d_pair(sA + stage * kHalfA, &B.tmA, fb, k0, it.z * kPairBM + rank * 128, it.y);
+          if (PHASE == kPhaseGemm) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              ptx::tma_load_3d_pair(sB + stage * kHalfB + q * (64 * kTcBK * 2), &B.tmB, fb,
+                                    it.w * kPairBN + rank * 128 + q * 64, k0, it.y);
+          } else {
+            ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, it.w * kPairBN + rank * 128, it.y);
+          }
+          ++issued[stage];
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // The leader's full barriers count both CTAs' bytes: once their last
+      // phases complete, no load of either CTA is still in flight.
+      if (leader) {
+        for (int s = 0; s < kStages; ++s) {
+          if (issued[s]) {
+            int zero = 0;
+            ptx::mbar_wait_cluster(&sh->full[s], (issued[s] - 1u) & 1u, &zero, p.status, p.timeout_ns);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer (leader only)
+      constexpr uint32_t idesc = ptx::idesc_bf16(kPairBM, kPairBN, PHASE == kPhaseGemm);
+      uint32_t stage = 0, phase = 0, local = 0;
+      bool ok = true;
+      for (int w = pair; w < p.n_items && ok; w += npairs, ++local) {
+        const int4 it = p.items[w];
+        const TcBucket& B = p.bk[it.x];
+        const int nk = (B.kdim + kTcBK - 1) / kTcBK;
+        const uint32_t acc = local & 1u;
+        if (!ptx::mbar_wait_cluster(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + acc * kPairBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(&sh->full[stage], phase, abortf, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(sA + stage * kHalfA);
+          const uint32_t b0 = ptx::smem_u32(sB + stage * kHalfB);
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const uint64_t adesc = ptx::sw128_desc(a0 + kk * 32, 16, 1024);
+            const uint64_t bdesc = (PHASE == kPhaseGemm) ? ptx::sw128_desc(b0 + kk * 2048, 64 * kTcBK * 2, 1024)
+                                                         : ptx::sw128_desc(b0 + kk * 32, 16, 1024);
+            ptx::umma_f16_pair(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_pair(&sh->empty[stage], 0x3);  // frees the stage in both CTAs
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit_pair(&sh->tfull[acc], 0x3);  // accumulator halves ready in both CTAs
+      }
+      ptx::umma_commit_pair(&sh->mma_done, 0x1);
+      int zero = 0;
+      ptx::mbar_wait(&sh->mma_done, 0, &zero, p.status, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t lead_tempty = ptx::mapa_shared(ptx::smem_u32(&sh->tempty[0]), 0);
+    uint32_t local = 0;
+    for (int w = pair; w < p.n_items; w += npairs, ++local) {
+      const uint32_t acc = local & 1u;
+      const int4 it = p.items[w];
+      const TcBucket& B = p.bk[it.x];
+      const int i = it.z * kPairBM + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const int jbase = it.w * kPairBN + half * (kPairBN / 2);
+      const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
+      const bf16* row = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
+      uint4 cur[4], nxt[4];
+      auto fetch = [&](int ch, uint4 (&dst)[4]) {
+        const int j0 = jbase + ch * 32;
+        if (need_aux && i < B.m && j0 + 32 <= lim) {
+          const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
+        }
+      };
+      fetch(0, cur);
+      fetch(1, nxt);
+      if (!ptx::mbar_wait_cluster(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
+      ptx::tc_fence_after();
+      const int gm = B.slot_mat[it.y];
+      const MatDev md = p.mats[gm];
+      float sc = 1.f;
+      if (p.first) {
+        const float s = p.s_norm[gm];
+        sc = (PHASE == kPhaseGram) ? s * s : s;
+      }
+      const uint32_t tbase = tmem + acc * kPairBN + half * (kPairBN / 2) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int ch = 0; ch < kEpiChunks; ++ch) {
+        float v[32];
+        ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
+        epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, jbase + ch * 32, sc, v, cur);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+        if (ch + 2 < kEpiChunks) fetch(ch + 2, nxt);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(lead_tempty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+    }
+  }
+
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+template <int PHASE>
+cudaError_t launch_pair_phase(const TcParams& p, int pairs, cudaStream_t s) {
+  const size_t smem = 1024 + kStages * (kHalfA + kHalfB) + sizeof(PairShared);
+  cudaError_t e = cudaFuncSetAttribute(tc_ns_pair_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_ns_pair_kernel<PHASE>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_pair(int phase, const TcParams& p, int pairs, cudaStream_t s) {
+  switch (phase) {
+    case kPhaseGram:
+      return launch_pair_phase<kPhaseGram>(p, pairs, s);
+    case kPhasePoly:
+      return launch_pair_phase<kPhasePoly>(p, pairs, s);
+    case kPhaseGemm:
+      return launch_pair_phase<kPhaseGemm>(p, pairs, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dmuon

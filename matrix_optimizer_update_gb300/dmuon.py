@@ -33,6 +33,7 @@ DTYPE = {"f32": F32, "bf16": BF16}
 FLAG_CAPTURE_UPDATE = 0x1
 FLAG_GRAM_NS = 0x2
 FLAG_TUNE = 0x4
+FLAG_PAIR_TILES = 0x8
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 

@@ -1,0 +1,58 @@
+"""GPU parity of the two-SM tile path (DMUON_FLAG_PAIR_TILES: 256 x 256 tiles
+on clusters of two CTAs, tcgen05 cta_group::2) against the fp64 oracle, in
+both iteration forms, plus bitwise agreement of repeated runs."""
+
+import pytest
+import torch
+
+from helpers import LibRun
+from test_gpu_parity import _check_all, _fill
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(300, 700), (700, 300), (520, 1000), (256, 1536), (1536, 256), (512, 512), (384, 384), (130, 130)]
+
+
+def test_pair_tiles_small():
+    run = LibRun([(256, 512), (512, 256)], pair=True)
+    d = run.muon.plan.describe()
+    assert all(b["pair"] for b in d["buckets"])
+    init = _fill(run, 5000)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    _check_all(run, init)
+
+
+@pytest.mark.parametrize("gram", [False, True])
+def test_pair_tiles_ragged(gram):
+    run = LibRun(SHAPES, pair=True, gram_ns=gram)
+    pairs = {(b["m"], b["n"]): b["pair"] for b in run.muon.plan.describe()["buckets"]}
+    assert pairs[(512, 512)] and pairs[(256, 1536)] and not pairs[(300, 700)] and not pairs[(130, 130)]
+    init = _fill(run, 5100, m_std=1e-3)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    worst = _check_all(run, init)
+    print("pair", "gram" if gram else "standard", worst)
+
+
+@pytest.mark.parametrize("ns_steps", [1, 2])
+def test_pair_tiles_step_counts(ns_steps):
+    run = LibRun([(256, 768), (768, 256), (512, 512)], pair=True, ns_steps=ns_steps)
+    init = _fill(run, 5200 + ns_steps)
+    run.step()
+    torch.cuda.synchronize()
+    _check_all(run, init, ns_steps=ns_steps)
+
+
+def test_pair_tiles_deterministic():
+    run = LibRun([(512, 1024), (1024, 512)], pair=True, capture=False)
+    _fill(run, 5300)
+    W0, M0 = run.W.clone(), run.M.clone()
+    run.step()
+    W1, M1 = run.W.clone(), run.M.clone()
+    run.W.copy_(W0)
+    run.M.copy_(M0)
+    run.step()
+    assert torch.equal(run.W, W1) and torch.equal(run.M, M1)
