@@ -240,3 +240,36 @@ def test_launch_count_per_step():
     c0 = run.muon.plan.launch_count()
     run.step()
     assert run.muon.plan.launch_count() - c0 == len(d["launches"]) == 1 + 2 * 3 * 5
+
+
+@pytest.mark.parametrize("flags", ["standard", "gram", "pair"])
+def test_cuda_graph_replay_matches_eager(flags):
+    # after one uncaptured step with the same pointers, dmuon_step records no host copies and can be
+    # captured; two graph replays must equal two eager steps bit for bit
+    shapes = [(512, 1024), (1024, 512), (256, 256)]
+    kw = {"gram_ns": flags == "gram", "pair": flags == "pair", "capture": False}
+    a = LibRun(shapes, **kw)
+    _fill(a, 6000, m_std=1e-3)
+    W0, M0 = a.W.clone(), a.M.clone()
+    a.step()
+    a.step()
+    torch.cuda.synchronize()
+    Wa, Ma = a.W.clone(), a.M.clone()
+    a.W.copy_(W0)
+    a.M.copy_(M0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        a.step()  # warm-up on the capture stream: uploads nothing new
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    a.W.copy_(W0)
+    a.M.copy_(M0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        a.muon.plan.step(a.ptrs(a.W), a.ptrs(a.G), a.ptrs(a.M), 0.02, 0.95, True, s.cuda_stream)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.W, Wa) and torch.equal(a.M, Ma)
