@@ -234,10 +234,13 @@ def run_ours(args):
     torch.cuda.set_device(local)
     build_mod.build()
     w = wl.get(args.workload)
-    if args.layers:
+    if args.layers or args.experts:
         import dataclasses
 
-        w = dataclasses.replace(w, layers=args.layers, name=f"{w.name}[{args.layers} layers]")
+        if args.layers:
+            w = dataclasses.replace(w, layers=args.layers, name=f"{w.name}[{args.layers} layers]")
+        if args.experts and w.experts:
+            w = dataclasses.replace(w, experts=args.experts, name=f"{w.name}[{args.experts} experts]")
     tot = wl.totals(w)
     ms = make_matrix_set(w, f"cuda:{local}", seed_offset=replica_seed_offset(rank))
     stream = torch.cuda.Stream()
@@ -474,6 +477,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0, help="truncate the workload to its first N layers (profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="truncate an MoE workload to N experts per layer (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")

@@ -96,6 +96,17 @@ typedef struct {
                                           256 x 256 tiles on pairs of SMs
                                           (two-SM UMMA, thread-block clusters of
                                           2). bf16 only.                        */
+#define DMUON_FLAG_EPILOGUE_AX 0x10u   /* standard form: add the a*X_k term of the
+                                          quintic step in the epilogue of the
+                                          product B X_k (reading the X_k tile),
+                                          with B = bA + cA^2. Without the flag
+                                          the step runs as X_{k+1} = P X_k with
+                                          P = aI + bA + cA^2 formed by the
+                                          symmetric-product epilogue (a on the
+                                          diagonal), and the last product reads
+                                          no X_k tile: the same polynomial, one
+                                          bf16 rounding of a + B_ii instead of
+                                          an fp32 a*X term.                      */
 #define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
                                           per bucket on the bound workspace, keep
                                           the faster, and order tiles by measured

@@ -176,12 +176,23 @@ double phase_flops(int kind, double m, double n) {
 
 int dtype_bytes(int32_t d) { return d == DMUON_BF16 ? 2 : 4; }
 
-// Default tile width for an output dimension of extent d: 256, unless the last
-// 256-wide tile would be at most half full, then 128.
-int32_t default_bn(int d) {
-  const int rem = d % 256;
-  return (rem != 0 && rem <= 128) ? 128 : 256;
+// Default tile widths. A 128 x 256 tile takes about 1.4x the time of a 128 x 128
+// one over the same K (it moves 48 KB of operands per 64-wide K slice against
+// 32 KB, for twice the flops; timed on the 1408-row MoE experts: the symmetric
+// products ran 66 tiles of 128 in 78 ms and 41 tiles of 256 in 66 ms). So 256
+// is the default unless its tiles, weighted by 1.4, outnumber those of 128.
+constexpr double kWideTileCost = 1.4;
+
+int64_t sym_tiles(int m, int bn) {  // tiles touching the upper triangle of m x m (128-row blocks)
+  const int64_t tn = cdiv(m, bn);
+  int64_t t = 0;
+  for (int64_t ti = 0; ti < cdiv(m, kTcBM); ++ti)  // column tiles tj with tj*bn + bn - 1 >= ti*128
+    t += tn - std::min<int64_t>(tn, (ti * kTcBM) / bn);
+  return t;
 }
+
+int32_t default_bn_sym(int m) { return kWideTileCost * sym_tiles(m, 256) <= sym_tiles(m, 128) ? 256 : 128; }
+int32_t default_bn_gemm(int n) { return kWideTileCost * cdiv(n, 256) <= cdiv(n, 128) ? 256 : 128; }
 
 // Tiles of one phase for one bucket, appended in cost order.
 void add_tiles(const dmuon_plan_s& P, int kind, int bucket_local, const BucketPlan& B, std::vector<int4>& out) {
@@ -235,8 +246,8 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].m_ld = static_cast<int32_t>(align_up(order[b].first, ld_mult));
     // the Gram-space form pays (>= 26% fewer flops) and keeps bf16 accuracy on wide matrices only
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
-    P.buckets[b].bn_sym = P.tc ? default_bn(order[b].first) : kSimtBN;
-    P.buckets[b].bn_gemm = P.tc ? default_bn(order[b].second) : kSimtBN;
+    P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
+    P.buckets[b].bn_gemm = P.tc ? default_bn_gemm(order[b].second) : kSimtBN;
     // two-SM 256 x 256 tiles where both dimensions fill them
     P.buckets[b].pair = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES) && order[b].first >= 256 &&
                         P.buckets[b].bn_sym == 256 && P.buckets[b].bn_gemm == 256;
@@ -448,7 +459,9 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   };
   const int S = P.ns_steps;
   auto cf = [&](int k, int q) { return P.coeffs[3 * k + q]; };
-  // standard form, step by step: A = X X^T; B = b A + c A A^T; X' = a X + B X (last: W update)
+  // standard form, step by step: A = X X^T; P = a I + b A + c A A^T; X' = P X (last: W update).
+  // With DMUON_FLAG_EPILOGUE_AX: B = b A + c A A^T and X' = a X + B X, a*X read in the epilogue.
+  const bool ax_epilogue = (P.flags & DMUON_FLAG_EPILOGUE_AX) != 0;
   for (int k = 0; k < S; ++k) {
     const int xin = (k & 1) ? kBufX1 : kBufX0, xout = (k & 1) ? kBufX0 : kBufX1;
     for (size_t ch = 0; ch < P.chunks.size(); ++ch)
@@ -457,11 +470,11 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
     for (size_t ch = 0; ch < P.chunks.size(); ++ch)
       if (!P.chunk_gram[ch])
         add(DMUON_KIND_POLY, kPhasePoly, k, (int)ch, kListPoly, kBufA, kBufA, kBufB, kBufA, 0, cf(k, 1), cf(k, 2),
-            0, 0, 0);
+            ax_epilogue ? 0.f : cf(k, 0), 0, 0);
     for (size_t ch = 0; ch < P.chunks.size(); ++ch)
       if (!P.chunk_gram[ch])
         add(DMUON_KIND_GEMM, kPhaseGemm, k, (int)ch, kListGemm, kBufB, xin, k == S - 1 ? kBufNone : xout, xin,
-            cf(k, 0), 0, 0, 0, k == 0, k == S - 1);
+            ax_epilogue ? cf(k, 0) : 0.f, 0, 0, 0, k == 0, k == S - 1);
   }
   // Gram-space form: G = X0 X0^T; per step P = a I + b G + c G^2, Q <- P Q, G <- (P G) P; X = Q X0
   for (size_t ch = 0; ch < P.chunks.size(); ++ch) {
@@ -693,7 +706,8 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (shapes == nullptr || n_mats <= 0) return fail(DMUON_ERR_INVALID_ARG, "empty matrix list");
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
-  if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES))
+  if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES |
+                DMUON_FLAG_EPILOGUE_AX))
     return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
@@ -1035,8 +1049,9 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
     const Launch& L = P->launches[l];
     snprintf(t, sizeof t,
              "%s{\"kind\": %d, \"step\": %d, \"chunk\": %d, \"bn\": %d, \"pair\": %s, \"grid\": %d, "
-             "\"work\": %.17g}",
-             l ? ", " : "", L.kind, L.step, L.chunk, L.bn, L.pair ? "true" : "false", L.grid, L.work);
+             "\"work\": %.17g, \"a\": %.9g, \"b\": %.9g, \"c\": %.9g, \"diag\": %.9g}",
+             l ? ", " : "", L.kind, L.step, L.chunk, L.bn, L.pair ? "true" : "false", L.grid, L.work, L.a, L.b,
+             L.c, L.diag);
     j += t;
   }
   j += "]}";

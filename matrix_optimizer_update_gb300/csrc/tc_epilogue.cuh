@@ -33,6 +33,11 @@ __device__ __forceinline__ void load_row_bf16(const bf16* src, int j0, int lim, 
   }
 }
 
+// STREAM: mark the stores evict-first (st.global.cs). The symmetric products'
+// outputs (A, B) are read again only by the next launch, after far more than
+// the L2 holds has streamed through it; marking them keeps the operand rows
+// that other CTAs are still reading in L2.
+template <bool STREAM>
 __device__ __forceinline__ void store_row_bf16(bf16* dst, int j0, int jmin, int lim, const float (&v)[32]) {
   if (j0 >= jmin && j0 + 32 <= lim) {
     uint4* d4 = reinterpret_cast<uint4*>(dst + j0);
@@ -42,7 +47,10 @@ __device__ __forceinline__ void store_row_bf16(bf16* dst, int j0, int jmin, int 
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
       for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
-      d4[q] = u;
+      if (STREAM)
+        __stcs(d4 + q, u);
+      else
+        d4[q] = u;
     }
   } else {
 #pragma unroll
@@ -93,11 +101,13 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
       for (int k = 0; k < 32; ++k) v[k] *= sc;
     }
     // own row: columns j >= i; mirror: (j, i) for j > i (coalesced across the warp's 32 rows)
-    store_row_bf16(out + (int64_t)i * B.out_ld, j0, i, m, v);
+    store_row_bf16<true>(out + (int64_t)i * B.out_ld, j0, i, m, v);
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       const int j = j0 + k;
-      if (j > i && j < m) out[(int64_t)j * B.out_ld + i] = __float2bfloat16_rn(v[k]);
+      if (j > i && j < m)
+        __stcs(reinterpret_cast<unsigned short*>(out + (int64_t)j * B.out_ld + i),
+               __bfloat16_as_ushort(__float2bfloat16_rn(v[k])));
     }
   } else {  // gemm
     const int m = B.m, n = B.n;
@@ -116,7 +126,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
     for (int k = 0; k < 32; ++k) v[k] = (p.a * x[k] + v[k]) * sc;
     if (!p.last) {
       bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride) + (int64_t)i * B.out_ld;
-      store_row_bf16(out, j0, 0, n, v);
+      store_row_bf16<false>(out, j0, 0, n, v);
       return;
     }
     // W update: every load of the chunk is issued before any store, so the

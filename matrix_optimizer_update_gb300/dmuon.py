@@ -34,6 +34,7 @@ FLAG_CAPTURE_UPDATE = 0x1
 FLAG_GRAM_NS = 0x2
 FLAG_TUNE = 0x4
 FLAG_PAIR_TILES = 0x8
+FLAG_EPILOGUE_AX = 0x10
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 

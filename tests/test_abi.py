@@ -5,6 +5,7 @@ counts tiles as stated."""
 import os
 import re
 
+import numpy as np
 import pytest
 
 from matrix_optimizer_update_gb300 import dmuon as dm
@@ -100,9 +101,11 @@ def test_plan_buckets_tiles_and_work(name):
     m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, b["bn_sym"], b["bn_gemm"])[1] for b in d["buckets"])
     for b in d["buckets"]:
         if w.compute == "bf16":
-            # 256-wide tiles unless the last one would be at most half full
-            for dim, key in ((b["m"], "bn_sym"), (b["n"], "bn_gemm")):
-                assert b[key] == (128 if 0 < dim % 256 <= 128 else 256), (b, key)
+            # 256-wide tiles unless 1.4x their count exceeds the count of 128-wide ones
+            sym = {bn: brute_tiles(b["m"], b["n"], bm, bn, bn)[0] for bn in (128, 256)}
+            gemm = {bn: brute_tiles(b["m"], b["n"], bm, bn, bn)[1] for bn in (128, 256)}
+            assert b["bn_sym"] == (256 if 1.4 * sym[256] <= sym[128] else 128), b
+            assert b["bn_gemm"] == (256 if 1.4 * gemm[256] <= gemm[128] else 128), b
     assert sum(c["gram"] for c in d["lists"]) == g_tot
     assert sum(c["poly"] for c in d["lists"]) == g_tot
     assert sum(c["gemm"] for c in d["lists"]) == m_tot
@@ -172,3 +175,24 @@ def test_costs_need_a_tuned_plan():
     with pytest.raises(dm.DmuonError) as e:
         p.costs()
     assert e.value.status == dm.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("ax", [False, True])
+def test_polynomial_coefficients_per_launch(ax):
+    """Standard form: the step's polynomial aX + (bA + cA^2)X is formed either as
+    P = aI + bA + cA^2 (a on the diagonal of the symmetric product, the last
+    product with a = 0) or, with FLAG_EPILOGUE_AX, with a*X in the last
+    product's epilogue. Per-step coefficients land on their own step."""
+    coeffs = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.0, -1.5, 0.5)]
+    p = dm.dmuon_plan([(256, 512), (512, 256)], 3, coeffs, flags=dm.FLAG_EPILOGUE_AX if ax else 0)
+    launches = p.describe()["launches"]
+    for L in launches[1:]:
+        a, b, c = (float(np.float32(x)) for x in coeffs[L["step"]])
+        if L["kind"] == dm.KIND_POLY:
+            assert (L["b"], L["c"]) == pytest.approx((b, c), rel=1e-7)
+            assert L["diag"] == pytest.approx(0.0 if ax else a, rel=1e-7)
+        elif L["kind"] == dm.KIND_GEMM:
+            assert L["a"] == pytest.approx(a if ax else 0.0, rel=1e-7)
+            assert L["diag"] == 0.0
+        else:
+            assert L["kind"] == dm.KIND_GRAM and L["a"] == 0.0 and L["diag"] == 0.0

@@ -91,10 +91,13 @@ def test_golden_tiny_step(compute):
             assert np.linalg.norm(W - Wr) / np.linalg.norm(Wr) <= 1e-6
 
 
+@pytest.mark.parametrize("epilogue_ax", [False, True], ids=["P_X", "aX_epilogue"])
 @pytest.mark.parametrize("compute", ["bf16", "f32"])
-def test_ragged_shapes(compute):
+def test_ragged_shapes(compute, epilogue_ax):
+    """Both forms of the quintic step: X' = P X with P = aI + bA + cA^2, and
+    X' = aX + (bA + cA^2) X with the a*X term in the last product's epilogue."""
     prm = "bf16" if compute == "bf16" else "f32"
-    run = LibRun(RAGGED, param=prm, grad=prm, compute=compute)
+    run = LibRun(RAGGED, param=prm, grad=prm, compute=compute, epilogue_ax=epilogue_ax)
     init = _fill(run, 500, grad_std=1e-3 if compute == "bf16" else 1.0, w_std=0.02 if compute == "bf16" else 1.0,
                  m_std=1e-3)
     run.step()

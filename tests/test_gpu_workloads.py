@@ -42,11 +42,15 @@ def sample_indices(w):
     return [i for i, m in enumerate(mats) if m[0] in (0, L - 1)]
 
 
-@pytest.mark.parametrize("name,gram,pair", [("qwen2.5-1.5b", False, False), ("llama-3.2-3b", False, False),
-                                            ("llama-3.1-8b", False, False), ("moe-16x64", False, False),
-                                            ("llama-3.1-8b", True, False), ("moe-16x64", True, False),
-                                            ("llama-3.1-8b", False, True)])
-def test_workload_parity(name, gram, pair):
+@pytest.mark.parametrize("name,gram,pair,ax", [("qwen2.5-1.5b", False, False, False),
+                                               ("llama-3.2-3b", False, False, False),
+                                               ("llama-3.1-8b", False, False, False),
+                                               ("moe-16x64", False, False, False),
+                                               ("llama-3.1-8b", True, False, False),
+                                               ("moe-16x64", True, False, False),
+                                               ("llama-3.1-8b", False, True, False),
+                                               ("llama-3.1-8b", False, False, True)])
+def test_workload_parity(name, gram, pair, ax):
     w = wl.get(name)
     ms = make_matrix_set(w, "cuda")
     idx = sample_indices(w)
@@ -55,7 +59,7 @@ def test_workload_parity(name, gram, pair):
     muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
                           grad=w.grad_dtype, compute=w.compute,
                           flags=dm.FLAG_CAPTURE_UPDATE | (dm.FLAG_GRAM_NS if gram else 0)
-                          | (dm.FLAG_PAIR_TILES if pair else 0))
+                          | (dm.FLAG_PAIR_TILES if pair else 0) | (dm.FLAG_EPILOGUE_AX if ax else 0))
     stream = torch.cuda.current_stream().cuda_stream
     muon.plan.step(ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M), w.lr, w.mu, w.nesterov, stream)
     torch.cuda.synchronize()
@@ -88,4 +92,5 @@ def test_workload_parity(name, gram, pair):
         assert ew <= TOL_W[w.param_dtype], (i, r, c, ew)
         assert em <= TOL_M, (i, r, c, em)
         assert weight_rounding_violations(Wg, Wr, W0, Xg, Xr, w.lr * ref.update_scale(r, c), w.param_dtype) == 0
-    print(name, "gram" if gram else "standard", "pair" if pair else "", "sampled", len(idx), "worst", worst)
+    print(name, "gram" if gram else "standard", "pair" if pair else "", "aX-epilogue" if ax else "", "sampled",
+          len(idx), "worst", worst)
