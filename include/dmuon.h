@@ -187,7 +187,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  * uncaptured call with the same pointers first so that none is needed.
  * Launches one momentum kernel, then 3*ns_steps kernels per chunk of
  * standard-form buckets and 4*ns_steps - 1 per chunk of Gram-space buckets
- * (a chunk: up to 8 buckets sharing form and tile widths); 1 + 1 kernels
+ * (a chunk: up to 7 buckets sharing form and tile widths); 1 + 1 kernels
  * when ns_steps == 0. dmuon_plan_describe lists them.
  */
 dmuon_status dmuon_step(dmuon_plan_t plan, void* const* params, const void* const* grads,

@@ -498,7 +498,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
 }
 
 dmuon_status make_map(CUtensorMap* map, const void* base, int inner, int rows, int count, int ld_elems,
-                      int box_inner, int box_rows) {
+                      int box_inner, int box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = get_encode_fn();
   if (enc == nullptr) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)count};
@@ -506,7 +506,7 @@ dmuon_status make_map(CUtensorMap* map, const void* base, int inner, int rows, i
   cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return DMUON_OK;
@@ -551,6 +551,10 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
     st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bn);
   if (st != DMUON_OK) return st;
   tb.kdim = (phase == kPhaseGemm) ? B.m : va.inner;
+  if (vo.base != nullptr) {  // epilogue stores: 32 x 32 boxes staged with a 64-byte swizzle
+    st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != DMUON_OK) return st;
+  }
   tb.out = vo.base;
   tb.out_mat_stride = vo.mat_bytes;
   tb.out_ld = vo.ld;

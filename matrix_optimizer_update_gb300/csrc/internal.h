@@ -10,7 +10,7 @@
 
 namespace dmuon {
 
-constexpr int kMaxBucketsPerLaunch = 8;
+constexpr int kMaxBucketsPerLaunch = 7;  // 7 x 512 B of bucket descriptors fit the 4 KB of launch parameters
 
 // Tensor-core tile: 128 rows (UMMA M) x 256 or 128 columns (UMMA N, chosen per
 // bucket), K staged 64 at a time.
@@ -73,6 +73,7 @@ struct StreamParams {
 struct TcBucket {
   CUtensorMap tmA;  // A operand: 128 x 64 boxes, K-major
   CUtensorMap tmB;  // B operand: 256 x 64 boxes K-major (gram/poly) or 64 x 64 boxes MN-major (gemm)
+  CUtensorMap tmOut;  // output: 32 x 32 boxes, 64-byte swizzle (epilogue TMA stores)
   const int32_t* slot_mat;  // slot -> global matrix index
   char* out;                // A (gram), B (poly), X_{k+1} (gemm, not last)
   const char* aux;          // A (poly: b*A term), X_k (gemm: a*X term)

@@ -74,6 +74,55 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&x)[3
   }
 }
 
+// ---- staging of a 32 x 32 bf16 box for a TMA store (64-byte rows, 64-byte
+// swizzle: the 16-byte piece c of row r sits at piece c ^ ((r >> 1) & 3)).
+// Lane r holds row r's 32 values (columns 0..31 of the box).
+__device__ __forceinline__ void stage_row_sw64(uint8_t* box, int r, const float (&v)[32]) {
+  uint8_t* row = box + r * 64;
+  const int x = (r >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+    *reinterpret_cast<uint4*>(row + ((c ^ x) << 4)) = u;
+  }
+}
+
+// The transpose: lane r's value k goes to row k, column r, so that the box
+// stored at (x = row origin, y = column origin) is the mirror image.
+__device__ __forceinline__ void stage_col_sw64(uint8_t* box, int r, const float (&v)[32]) {
+  const int c = r >> 3, off = (r & 7) * 2;
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    *reinterpret_cast<bf16*>(box + k * 64 + ((c ^ ((k >> 1) & 3)) << 4) + off) = __float2bfloat16_rn(v[k]);
+}
+
+// Values of a chunk that lies strictly above the diagonal of a symmetric
+// product (so no diagonal term): gram s^2-scaled (sc), poly b*A + c*(A A^T).
+template <int PHASE>
+__device__ __forceinline__ void sym_values(const TcParams& p, const TcBucket& B, int slot, int i, int j0, float sc,
+                                           float (&v)[32], const uint4 (&pre)[4]) {
+  if (PHASE == kPhasePoly) {
+    float a[32];
+    if (i >= B.m) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) a[k] = 0.f;
+    } else if (j0 + 32 <= B.m) {
+      unpack_bf16x32(pre, a);
+    } else {
+      const bf16* A = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      load_row_bf16(A, j0, B.m, a);
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = p.b * a[k] + p.c * v[k];
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] *= sc;
+  }
+}
+
 // Epilogue of one 32-column chunk of one accumulator row. `pre` holds the
 // chunk's bf16 operand of the linear term (A for poly, X_k for gemm) when the
 // whole chunk lies inside the matrix (fetched before the accumulator was

@@ -46,6 +46,7 @@ using bf16 = __nv_bfloat16;
 
 constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 16 KB: 128 rows x 128 B
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
+constexpr int kStageBox = 32 * 32 * 2;            // one 32 x 32 bf16 box staged for a TMA store
 
 // Tile width N of one CTA (the UMMA N): 256, or 128 for buckets whose edges
 // would leave much of a 256-wide tile empty. Shared-memory stages fill the
@@ -69,6 +70,8 @@ struct TcShared {
   int abort_flag;
 };
 
+static_assert(sizeof(TcShared<6>) <= 1024, "barriers must fit their 1 KB");
+
 template <int PHASE, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<BN>;
@@ -81,6 +84,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   uint8_t* sA = base;
   uint8_t* sB = base + kTcStages * kStageA;
   TcShared<kTcStages>* sh = reinterpret_cast<TcShared<kTcStages>*>(sB + kTcStages * kStageB);
+  // Epilogue staging for TMA stores: two 2 KB boxes (32 x 32 bf16) per epilogue warp, after the
+  // barriers' 1 KB.
+  uint8_t* stg_all = sB + kTcStages * kStageB + 1024;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abortf = &sh->abort_flag;
@@ -206,7 +212,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     // Two warps per TMEM lane quarter (warp % 4), each on one half of the 256 columns.
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    uint32_t local = 0;
+    uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
+    uint32_t local = 0, nbox = 0;
     for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++local) {
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
@@ -241,11 +248,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         sc = (PHASE == kPhaseGram) ? s * s : s;
       }
       const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
+      // Output chunks leave through shared memory and TMA stores (one 32 x 32 box per chunk, and
+      // its mirror image for the symmetric products): X' of the gemm (not on the last step, which
+      // updates W, nor when a*X is added here), and every chunk of a symmetric product strictly
+      // above the diagonal. Diagonal chunks, the W update and the capture take the per-row path.
+      const int i0 = it.z * kTcBM + q * 32;
+      const bool gemm_tma = PHASE == kPhaseGemm && !p.last && !need_aux;
 #pragma unroll 1
       for (int ch = 0; ch < kEpiChunks; ++ch) {
         float v[32];
         ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
-        epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, jbase + ch * 32, sc, v, cur);
+        const int j0 = jbase + ch * 32;
+        if (PHASE == kPhaseGemm && gemm_tma) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] *= sc;
+          uint8_t* box = stg + (nbox & 1u) * kStageBox;
+          if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this box is done with it
+          __syncwarp();
+          epi::stage_row_sw64(box, lane, v);
+          ptx::fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            if (i0 < B.m && j0 < B.n) ptx::tma_store_3d(&B.tmOut, box, j0, i0, it.y);
+            ptx::bulk_commit();  // one group per box, stored or not, so the count above holds
+          }
+          ++nbox;
+        } else if (PHASE != kPhaseGemm && j0 >= i0 + 32 && i0 < B.m && j0 < B.m) {
+          epi::sym_values<PHASE>(p, B, it.y, i, j0, sc, v, cur);
+          if (lane == 0) ptx::bulk_wait_read<0>();
+          __syncwarp();
+          epi::stage_row_sw64(stg, lane, v);
+          epi::stage_col_sw64(stg + kStageBox, lane, v);
+          ptx::fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&B.tmOut, stg, j0, i0, it.y);
+            ptx::tma_store_3d(&B.tmOut, stg + kStageBox, i0, j0, it.y);
+            ptx::bulk_commit();
+          }
+        } else {
+          epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
         if (ch + 2 < kEpiChunks) fetch(ch + 2, nxt);
@@ -254,6 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->tempty[acc]);
     }
+    if (lane == 0) ptx::bulk_wait_all();  // every TMA store of this warp has landed
   }
 
   __syncthreads();
@@ -267,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
 template <int PHASE, int BN>
 size_t smem_bytes() {
   using C = TcCfg<BN>;
-  return 1024 + C::kStages * (kStageA + C::kStageB) + sizeof(TcShared<C::kStages>);
+  return 1024 + C::kStages * (kStageA + C::kStageB) + 1024 + kEpiWarps * kStageBox * 2;
 }
 
 template <int PHASE, int BN>

@@ -125,12 +125,24 @@ def test_plan_buckets_tiles_and_work(name):
     assert p.workspace_bytes() > 0
 
 
+MAX_BUCKETS_PER_LAUNCH = 7
+
+
 def test_many_buckets_split_into_chunks():
+    """Buckets with the same iteration form and tile widths share a launch, at
+    most seven to a launch (the bucket descriptors fill the 4 KB of launch
+    parameters)."""
     shapes = [(16 * (k + 1), 256) for k in range(19)]
     p = dm.dmuon_plan(shapes, 2)
     d = p.describe()
-    assert d["chunks"] == 3 and len(d["buckets"]) == 19
-    assert len(d["launches"]) == 1 + 3 * 2 * 3
+    assert len(d["buckets"]) == 19
+    groups = {}
+    for b in d["buckets"]:
+        key = (b["bn_sym"], b["bn_gemm"])
+        groups[key] = groups.get(key, 0) + 1
+    want = sum(cdiv(n, MAX_BUCKETS_PER_LAUNCH) for n in groups.values())
+    assert len(groups) == 2 and d["chunks"] == want == 4
+    assert len(d["launches"]) == 1 + 3 * 2 * want
 
 
 def test_ns_steps_zero_plan():
