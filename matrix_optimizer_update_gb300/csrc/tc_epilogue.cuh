@@ -123,6 +123,111 @@ __device__ __forceinline__ void sym_values(const TcParams& p, const TcBucket& B,
   }
 }
 
+// ---- last step on bf16 weights: W -= lr * scale * X, one 32 x 32 chunk of X
+// (rows i0.., columns j0.. in the iteration's orientation) at a time. The
+// chunk's W block is copied into shared memory ahead of time (cp.async, 16
+// bytes per lane and row segment), updated there row by row from the fp32 X
+// each lane holds (one rounding per element), and written back with
+// coalesced 16-byte stores. Box layout: 32 rows of 64 bytes, piece c of row
+// r at piece c ^ ((r >> 1) & 3). Box rows are W rows: i0 + r for W = m x n,
+// j0 + r for W = n x m (stored transposed).
+
+// Whole chunk inside W with 16-byte aligned row segments (else the per-row path).
+__device__ __forceinline__ bool w_chunk_vec(const MatDev& md, int m, int n, int i0, int j0) {
+  return md.transposed ? ((m & 7) == 0 && i0 + 32 <= m && j0 < n) : ((n & 7) == 0 && j0 + 32 <= n && i0 < m);
+}
+
+// Offset of the 16-byte W segment that lane copies for box row rr, or -1 past W's edge.
+__device__ __forceinline__ int64_t w_seg(const MatDev& md, int m, int n, int i0, int j0, int rr, int pc) {
+  if (md.transposed) return (j0 + rr < n) ? (int64_t)(j0 + rr) * m + i0 + 8 * pc : -1;
+  return (i0 + rr < m) ? (int64_t)(i0 + rr) * n + j0 + 8 * pc : -1;
+}
+
+__device__ __forceinline__ uint8_t* box_piece(uint8_t* box, int r, int c) {
+  return box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ void w_chunk_fetch(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
+                                              int j0, int lane, uint8_t* box) {
+  if (!w_chunk_vec(md, m, n, i0, j0)) return;
+  const bf16* W = reinterpret_cast<const bf16*>(p.ptrs[gm]);
+  const int pc = lane & 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int rr = (lane >> 2) + 8 * u;
+    const int64_t off = w_seg(md, m, n, i0, j0, rr, pc);
+    if (off >= 0) ptx::cp_async16(box_piece(box, rr, pc), W + off);
+  }
+}
+
+// The copies of this chunk must have landed (cp_async_wait + __syncwarp) before the call.
+__device__ __forceinline__ void w_chunk_apply(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
+                                              int j0, int lane, const float (&v)[32], uint8_t* box) {
+  const float step = p.lr * md.scale;
+  if (!md.transposed) {  // box row = this lane's row
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4* pp = reinterpret_cast<uint4*>(box_piece(box, lane, c));
+      uint4 u = *pp;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(h[e]);
+        f.x -= step * v[8 * c + 2 * e];
+        f.y -= step * v[8 * c + 2 * e + 1];
+        h[e] = __floats2bfloat162_rn(f.x, f.y);
+      }
+      *pp = u;
+    }
+  } else {  // box column = this lane's row: element (k, lane)
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      bf16* e = reinterpret_cast<bf16*>(box_piece(box, k, lane >> 3)) + (lane & 7);
+      *e = __float2bfloat16_rn(__bfloat162float(*e) - step * v[k]);
+    }
+  }
+  __syncwarp();
+  bf16* W = reinterpret_cast<bf16*>(p.ptrs[gm]);
+  const int pc = lane & 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int rr = (lane >> 2) + 8 * u;
+    const int64_t off = w_seg(md, m, n, i0, j0, rr, pc);
+    if (off >= 0) *reinterpret_cast<uint4*>(W + off) = *reinterpret_cast<const uint4*>(box_piece(box, rr, pc));
+  }
+  __syncwarp();
+}
+
+// The linear term and the normalisation of the last product's chunk: v = (a x + v) s.
+__device__ __forceinline__ void gemm_values(const TcParams& p, const TcBucket& B, int slot, int i, int j0, float sc,
+                                            float (&v)[32], const uint4 (&pre)[4]) {
+  if (p.a != 0.f && i < B.m) {
+    float x[32];
+    if (j0 + 32 <= B.n) {
+      unpack_bf16x32(pre, x);
+    } else {
+      const bf16* X = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      load_row_bf16(X, j0, B.n, x);
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = (p.a * x[k] + v[k]) * sc;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] *= sc;
+  }
+}
+
+__device__ __forceinline__ void capture_row(const TcParams& p, const MatDev& md, int i, int j0, int m, int n,
+                                            const float (&v)[32]) {
+  if (p.capture == nullptr || md.cap_off < 0 || i >= m) return;
+  float* cap = p.capture + md.cap_off;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int j = j0 + k;
+    if (j < n) cap[md.transposed ? (int64_t)j * m + i : (int64_t)i * n + j] = v[k];
+  }
+}
+
 // Epilogue of one 32-column chunk of one accumulator row. `pre` holds the
 // chunk's bf16 operand of the linear term (A for poly, X_k for gemm) when the
 // whole chunk lies inside the matrix (fetched before the accumulator was

@@ -238,10 +238,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       };
       fetch(0, cur);
       fetch(1, nxt);
-      if (!ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
-      ptx::tc_fence_after();
       const int gm = B.slot_mat[it.y];
       const MatDev md = p.mats[gm];
+      const int i0 = it.z * kTcBM + q * 32;
+      // last step on bf16 weights: the W blocks of the first two chunks are copied in while the
+      // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
+      const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
+      if (w_last) {
+        epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase, lane, stg);
+        ptx::cp_async_commit();
+        epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase + 32, lane, stg + kStageBox);
+        ptx::cp_async_commit();
+      }
+      if (!ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
+      ptx::tc_fence_after();
       float sc = 1.f;
       if (p.first) {
         const float s = p.s_norm[gm];
@@ -251,8 +261,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       // Output chunks leave through shared memory and TMA stores (one 32 x 32 box per chunk, and
       // its mirror image for the symmetric products): X' of the gemm (not on the last step, which
       // updates W, nor when a*X is added here), and every chunk of a symmetric product strictly
-      // above the diagonal. Diagonal chunks, the W update and the capture take the per-row path.
-      const int i0 = it.z * kTcBM + q * 32;
+      // above the diagonal. On the last step bf16 weights are updated in shared memory from
+      // prefetched blocks. Diagonal chunks, matrix edges and fp32 weights take the per-row path.
       const bool gemm_tma = PHASE == kPhaseGemm && !p.last && !need_aux;
 #pragma unroll 1
       for (int ch = 0; ch < kEpiChunks; ++ch) {
@@ -273,6 +283,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
             ptx::bulk_commit();  // one group per box, stored or not, so the count above holds
           }
           ++nbox;
+        } else if (PHASE == kPhaseGemm && w_last) {
+          uint8_t* box = stg + (ch & 1) * kStageBox;
+          ptx::cp_async_wait<1>();  // this chunk's copies (all but the newest group) have landed
+          __syncwarp();
+          if (epi::w_chunk_vec(md, B.m, B.n, i0, j0)) {
+            epi::gemm_values(p, B, it.y, i, j0, sc, v, cur);
+            epi::capture_row(p, md, i, j0, B.m, B.n, v);
+            epi::w_chunk_apply(p, md, gm, B.m, B.n, i0, j0, lane, v, box);
+          } else {
+            epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);  // matrix edges
+          }
+          if (ch + 2 < kEpiChunks) epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
+          ptx::cp_async_commit();
         } else if (PHASE != kPhaseGemm && j0 >= i0 + 32 && i0 < B.m && j0 < B.m) {
           epi::sym_values<PHASE>(p, B, it.y, i, j0, sc, v, cur);
           if (lane == 0) ptx::bulk_wait_read<0>();
@@ -298,6 +321,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       if (lane == 0) ptx::mbar_arrive(&sh->tempty[acc]);
     }
     if (lane == 0) ptx::bulk_wait_all();  // every TMA store of this warp has landed
+    ptx::cp_async_wait<0>();              // and every W copy (matters only after an abort)
   }
 
   __syncthreads();
