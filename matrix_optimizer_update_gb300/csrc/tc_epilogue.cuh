@@ -99,27 +99,60 @@ __device__ __forceinline__ void stage_col_sw64(uint8_t* box, int r, const float 
     *reinterpret_cast<bf16*>(box + k * 64 + ((c ^ ((k >> 1) & 3)) << 4) + off) = __float2bfloat16_rn(v[k]);
 }
 
-// Values of a chunk that lies strictly above the diagonal of a symmetric
-// product (so no diagonal term): gram s^2-scaled (sc), poly b*A + c*(A A^T).
-template <int PHASE>
-__device__ __forceinline__ void sym_values(const TcParams& p, const TcBucket& B, int slot, int i, int j0, float sc,
-                                           float (&v)[32], const uint4 (&pre)[4]) {
-  if (PHASE == kPhasePoly) {
-    float a[32];
-    if (i >= B.m) {
+// Poly's b*A operand of one chunk as this lane's row (a[k] = A[i][j0 + k]).
+// `blk` holds the chunk's 32 x 32 block of A as fetched (lane: row
+// (lane >> 2) + 8u, piece lane & 3); it is turned into rows through `box`
+// (64-byte swizzled rows), which must be free. Chunks past the matrix's
+// right edge read their row directly.
+__device__ __forceinline__ void poly_aux_rows(const TcBucket& B, const bf16* abase, int i, int j0, int lane,
+                                              const uint4 (&blk)[4], uint8_t* box, float (&a)[32]) {
+  if (j0 + 32 <= B.m) {
+    const int i0 = i - lane;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) a[k] = 0.f;
-    } else if (j0 + 32 <= B.m) {
-      unpack_bf16x32(pre, a);
-    } else {
-      const bf16* A = reinterpret_cast<const bf16*>(B.aux + slot * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
-      load_row_bf16(A, j0, B.m, a);
+    for (int u = 0; u < 4; ++u) {
+      const int rr = (lane >> 2) + 8 * u;
+      if (i0 + rr < B.m) *reinterpret_cast<uint4*>(box + rr * 64 + (((lane & 3) ^ ((rr >> 1) & 3)) << 4)) = blk[u];
     }
+    __syncwarp();
+    uint4 r[4];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = p.b * a[k] + p.c * v[k];
+    for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const uint4*>(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+    unpack_bf16x32(r, a);
+    __syncwarp();  // every lane has its row before the box is reused
+  } else if (i < B.m) {
+    load_row_bf16(abase + (int64_t)i * B.aux_ld, j0, B.m, a);
   } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] *= sc;
+    for (int k = 0; k < 32; ++k) a[k] = 0.f;
+  }
+}
+
+// Values of a chunk strictly above the diagonal (no diagonal term): gram
+// s^2-scaled (sc), poly b*A + c*(A A^T).
+template <int PHASE>
+__device__ __forceinline__ void sym_values(const TcParams& p, float sc, const float (&a)[32], float (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = (PHASE == kPhasePoly) ? p.b * a[k] + p.c * v[k] : v[k] * sc;
+}
+
+// A chunk on the diagonal: values with the diagonal term, then the own row
+// for columns j >= i and the mirror (j, i) for j > i, per element.
+template <int PHASE>
+__device__ __forceinline__ void sym_diag_chunk(const TcParams& p, const TcBucket& B, int slot, int i, int j0,
+                                               float sc, const float (&a)[32], float (&v)[32]) {
+  const int m = B.m;
+  if (i >= m) return;
+#pragma unroll
+  for (int k = 0; k < 32; ++k)
+    v[k] = (PHASE == kPhasePoly) ? p.b * a[k] + p.c * v[k] + (j0 + k == i ? p.diag : 0.f) : v[k] * sc;
+  bf16* out = reinterpret_cast<bf16*>(B.out + slot * B.out_mat_stride);
+  store_row_bf16<true>(out + (int64_t)i * B.out_ld, j0, i, m, v);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int j = j0 + k;
+    if (j > i && j < m)
+      __stcs(reinterpret_cast<unsigned short*>(out + (int64_t)j * B.out_ld + i),
+             __bfloat16_as_ushort(__float2bfloat16_rn(v[k])));
   }
 }
 

@@ -218,19 +218,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
-      const int i = it.z * kTcBM + q * 32 + lane;
+      const int i0 = it.z * kTcBM + q * 32;
+      const int i = i0 + lane;
       const int jbase = it.w * BN + half * (BN / 2);
       // The linear term's operand does not depend on the accumulator: the first
       // two chunks are fetched while the MMAs of this tile are still running,
       // each later chunk while the chunk two places before it is processed.
+      // Poly (b*A): the chunk's 32 x 32 block of A, coalesced (lane: row
+      // (lane >> 2) + 8u, 16-byte piece lane & 3), only where the chunk touches
+      // the upper triangle. Gemm with a*X in the epilogue: this lane's row.
       const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
-      const bf16* row = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
+      const bf16* abase = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride);
+      const bf16* row = abase + (int64_t)i * B.aux_ld;
       // gemm with a == 0 (the last product of the Gram-space recurrence) has no linear term
       const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
       uint4 cur[4], nxt[4];
       auto fetch = [&](int ch, uint4 (&dst)[4]) {
         const int j0 = jbase + ch * 32;
-        if (need_aux && i < B.m && j0 + 32 <= lim) {
+        if (PHASE == kPhasePoly) {
+          if (j0 + 32 <= B.m && j0 + 31 >= i0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int ii = i0 + (lane >> 2) + 8 * u;
+              if (ii < B.m)
+                dst[u] = __ldg(reinterpret_cast<const uint4*>(abase + (int64_t)ii * B.aux_ld + j0 + 8 * (lane & 3)));
+            }
+          }
+        } else if (need_aux && i < B.m && j0 + 32 <= lim) {
           const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
@@ -240,7 +254,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       fetch(1, nxt);
       const int gm = B.slot_mat[it.y];
       const MatDev md = p.mats[gm];
-      const int i0 = it.z * kTcBM + q * 32;
       // last step on bf16 weights: the W blocks of the first two chunks are copied in while the
       // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
       const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
@@ -296,20 +309,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           }
           if (ch + 2 < kEpiChunks) epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
           ptx::cp_async_commit();
-        } else if (PHASE != kPhaseGemm && j0 >= i0 + 32 && i0 < B.m && j0 < B.m) {
-          epi::sym_values<PHASE>(p, B, it.y, i, j0, sc, v, cur);
-          if (lane == 0) ptx::bulk_wait_read<0>();
+        } else if (PHASE != kPhaseGemm && i0 < B.m && j0 < B.m && j0 + 31 >= i0) {
+          // a chunk of a symmetric product touching the upper triangle
+          if (lane == 0) ptx::bulk_wait_read<0>();  // both boxes free again
           __syncwarp();
-          epi::stage_row_sw64(stg, lane, v);
-          epi::stage_col_sw64(stg + kStageBox, lane, v);
-          ptx::fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_3d(&B.tmOut, stg, j0, i0, it.y);
-            ptx::tma_store_3d(&B.tmOut, stg + kStageBox, i0, j0, it.y);
-            ptx::bulk_commit();
+          float a[32];
+          if (PHASE == kPhasePoly) epi::poly_aux_rows(B, abase, i, j0, lane, cur, stg, a);
+          if (j0 >= i0 + 32) {  // strictly above the diagonal: the chunk and its mirror as TMA boxes
+            epi::sym_values<PHASE>(p, sc, a, v);
+            epi::stage_row_sw64(stg, lane, v);
+            epi::stage_col_sw64(stg + kStageBox, lane, v);
+            ptx::fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&B.tmOut, stg, j0, i0, it.y);
+              ptx::tma_store_3d(&B.tmOut, stg + kStageBox, i0, j0, it.y);
+              ptx::bulk_commit();
+            }
+          } else {  // on the diagonal: per-row stores keep the result exactly symmetric
+            epi::sym_diag_chunk<PHASE>(p, B, it.y, i, j0, sc, a, v);
           }
-        } else {
+        } else if (PHASE == kPhaseGemm) {
           epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);
         }
 #pragma unroll
