@@ -118,13 +118,14 @@ typedef struct {
                                           kernel returned early, results invalid */
 
 /* Launch kinds reported by the profiler. */
-#define DMUON_KIND_MOMENTUM 0 /* momentum + sum of squares + cast/transposed copy */
+#define DMUON_KIND_MOMENTUM 0 /* momentum + per-unit sums of squares + cast/transposed copy */
 #define DMUON_KIND_GRAM 1     /* A = X X^T, upper tiles, mirrored                  */
 #define DMUON_KIND_POLY 2     /* B = b*A + c*A A^T, upper tiles, mirrored          */
 #define DMUON_KIND_GEMM 3     /* X' = a*X + B X (last step: W update epilogue)     */
 #define DMUON_KIND_UPDATE0 4  /* W update straight from U (ns_steps == 0)          */
 #define DMUON_KIND_SYMM 5     /* Gram-space form: product of two commuting
                                  symmetric m x m matrices, upper tiles, mirrored   */
+#define DMUON_KIND_NORM 6     /* s = 1/(||U||_F + eps) per matrix from the partials */
 
 typedef struct dmuon_plan_s* dmuon_plan_t;
 
@@ -185,10 +186,11 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  * pointers differs from the previous call's it is uploaded with a
  * cudaMemcpyAsync from host memory; under CUDA-graph capture, make one
  * uncaptured call with the same pointers first so that none is needed.
- * Launches one momentum kernel, then 3*ns_steps kernels per chunk of
- * standard-form buckets and 4*ns_steps - 1 per chunk of Gram-space buckets
- * (a chunk: up to 7 buckets sharing form and tile widths); 1 + 1 kernels
- * when ns_steps == 0. dmuon_plan_describe lists them.
+ * Launches the momentum kernel and the per-matrix norm kernel, then
+ * 3*ns_steps kernels per chunk of standard-form buckets and 4*ns_steps - 1
+ * per chunk of Gram-space buckets (a chunk: up to 7 buckets sharing form and
+ * tile widths); 2 + 1 kernels when ns_steps == 0. dmuon_plan_describe lists
+ * them.
  */
 dmuon_status dmuon_step(dmuon_plan_t plan, void* const* params, const void* const* grads,
                         void* const* momenta, float lr, float mu, int32_t nesterov, void* stream);

@@ -134,7 +134,7 @@ struct dmuon_plan_s {
   std::vector<Launch> launches;
   // ---- workspace layout (byte offsets)
   size_t ws_bytes = 0;
-  int64_t off_status = 0, off_counters = 0, off_s = 0, off_partial = 0, off_mats = 0, off_ub = 0, off_ptrs = 0,
+  int64_t off_status = 0, off_s = 0, off_partial = 0, off_mats = 0, off_ub = 0, off_ptrs = 0,
           off_items = 0, off_probe = 0, off_capture = -1;
   int64_t cap_elems = 0;
   // ---- binding
@@ -368,7 +368,6 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
     return o;
   };
   P.off_status = take(256);
-  P.off_counters = take(4LL * n_mats);
   P.off_s = take(4LL * n_mats);
   P.off_partial = take(4LL * std::max<int64_t>(units, 1));
   P.off_mats = take((int64_t)sizeof(MatDev) * n_mats);
@@ -425,6 +424,10 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   L.kind = DMUON_KIND_MOMENTUM;
   L.work = elems * (gb + 4 + 4 + P.xel);
   P.launches.push_back(L);
+  Launch nf;
+  nf.kind = DMUON_KIND_NORM;
+  nf.work = 4.0 * static_cast<double>(P.n_units) + 4.0 * n_mats;  // partials read, s written
+  P.launches.push_back(nf);
   if (P.ns_steps == 0) {
     Launch u;
     u.kind = DMUON_KIND_UPDATE0;
@@ -810,7 +813,6 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   sp.ptrs = reinterpret_cast<const uint64_t*>(ws + P->off_ptrs);
   sp.ws = ws;
   sp.partial = reinterpret_cast<float*>(ws + P->off_partial);
-  sp.counters = reinterpret_cast<unsigned*>(ws + P->off_counters);
   sp.s_norm = reinterpret_cast<float*>(ws + P->off_s);
   sp.status = reinterpret_cast<unsigned*>(ws + P->off_status);
   sp.capture = P->off_capture >= 0 ? reinterpret_cast<float*>(ws + P->off_capture) : nullptr;
@@ -838,6 +840,10 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
     if (L.kind == DMUON_KIND_MOMENTUM || L.kind == DMUON_KIND_UPDATE0) {
       const int per_sm = (L.kind == DMUON_KIND_MOMENTUM) ? momentum_blocks_per_sm(sp.grad_bf16, sp.x_bf16) : 4;
       L.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(P->n_units, (int64_t)per_sm * P->num_sms)));
+      continue;
+    }
+    if (L.kind == DMUON_KIND_NORM) {  // one CTA per matrix, up to 8 per SM
+      L.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(P->shapes.size(), 8LL * P->num_sms)));
       continue;
     }
     const std::vector<int>& ch = P->chunks[L.chunk];
@@ -975,6 +981,8 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     if (st != DMUON_OK) return st;
     if (L.kind == DMUON_KIND_MOMENTUM) {
       e = launch_momentum(sp, L.grid, s);
+    } else if (L.kind == DMUON_KIND_NORM) {
+      e = launch_norm_finalize(sp, L.grid, s);
     } else if (L.kind == DMUON_KIND_UPDATE0) {
       e = launch_update0(sp, L.grid, s);
     } else if (P->tc) {

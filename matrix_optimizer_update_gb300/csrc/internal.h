@@ -57,8 +57,7 @@ struct StreamParams {
   const int64_t* unit_begin;  // [n_mats + 1]
   const uint64_t* ptrs;       // [3 * n_mats]: W, G, M device pointers
   char* ws;
-  float* partial;             // [n_units]
-  unsigned* counters;         // [n_mats], zero between launches
+  float* partial;             // [n_units]: each unit's sum of squares of U
   float* s_norm;              // [n_mats]: 1 / (||U||_F + eps)
   unsigned* status;
   float* capture;
@@ -128,6 +127,7 @@ struct SimtParams {
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s);
+cudaError_t launch_norm_finalize(const StreamParams& p, int grid, cudaStream_t s);
 cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s);
 int momentum_blocks_per_sm(int grad_bf16, int x_bf16);  // resident CTAs per SM of the momentum kernel
 cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream_t s);

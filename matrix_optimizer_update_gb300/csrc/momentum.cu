@@ -4,10 +4,12 @@
 //   M <- mu*M + G;  U = G + mu*M (Nesterov) or U = M      (fp32 math, M in place)
 //   U is written to the matrix's workspace slot in the compute dtype, already
 //   in the short-side orientation (transposed through shared memory when
-//   rows > cols), and sum(U^2) is reduced per matrix, deterministically:
-//   each work unit writes one fp32 partial, and the CTA that finishes a
-//   matrix's last unit (an atomic ticket, no waiting) adds that matrix's
-//   partials in a fixed order in fp64 and stores s = 1 / (sqrt(sum) + eps).
+//   rows > cols), and each work unit writes its fp32 partial of sum(U^2).
+// A second, small launch (norm_finalize_kernel) adds each matrix's partials
+// in a fixed order in fp64 and stores s = 1 / (sqrt(sum) + eps): the sum is
+// deterministic, and the streaming pass carries no fence or atomic per unit
+// (a ticket per unit, with the fence it needs, cost about a third of the
+// pass's bandwidth).
 // The Newton-Schulz kernels fold s into their first-step epilogues, so U is
 // never rescaled in HBM. ("momentum-aggregated gradients", "DMuon: Efficient
 // Distributed Muon Training with Near-Adam Overhead", gist.science summary
@@ -112,8 +114,6 @@ template <bool GB, bool XB>
 __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_constant__ StreamParams p) {
   __shared__ float tileU[kTileR][kTileC + 1];
   __shared__ float redf[kStreamThreads / 32];
-  __shared__ double redd[kStreamThreads / 32];
-  __shared__ int is_last;
   const float mu = p.mu;
   const bool nest = p.nesterov != 0;
 
@@ -258,29 +258,30 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
       }
     }
 
-    // per-unit partial, then the last unit of the matrix finalises s
+    // the unit's partial sum of squares (the sum over the matrix is the finalize launch's)
     const float bs = block_sum_f(ss, redf);
+    if (threadIdx.x == 0) p.partial[u] = bs;
+    __syncthreads();  // redf is reused by the next unit
+  }
+}
+
+// s = 1 / (||U||_F + eps) per matrix from its units' partials, added in fp64
+// in a fixed order (thread t takes partials t, t + 256, ...; then a fixed
+// tree), so the result does not depend on the launch configuration.
+__global__ void __launch_bounds__(kStreamThreads) norm_finalize_kernel(const __grid_constant__ StreamParams p) {
+  __shared__ double redd[kStreamThreads / 32];
+  for (int mat = blockIdx.x; mat < p.n_mats; mat += gridDim.x) {
+    const MatDev md = p.mats[mat];
+    double acc = 0.0;
+    for (int64_t k = threadIdx.x; k < md.unit_count; k += kStreamThreads)
+      acc += static_cast<double>(p.partial[md.unit_begin + k]);
+    const double tot = block_sum_d(acc, redd);
     if (threadIdx.x == 0) {
-      p.partial[u] = bs;
-      __threadfence();
-      const unsigned t = atomicAdd(&p.counters[mat], 1u);
-      is_last = (t == static_cast<unsigned>(md.unit_count - 1));
+      const float nrm = static_cast<float>(sqrt(tot));
+      if (!isfinite(nrm)) atomicOr(p.status, DMUON_DEV_NONFINITE_NORM);
+      p.s_norm[mat] = 1.0f / (nrm + p.eps);
     }
-    __syncthreads();
-    if (is_last) {
-      __threadfence();
-      double acc = 0.0;
-      for (int64_t k = threadIdx.x; k < md.unit_count; k += kStreamThreads)
-        acc += static_cast<double>(__ldcg(&p.partial[md.unit_begin + k]));
-      const double tot = block_sum_d(acc, redd);
-      if (threadIdx.x == 0) {
-        const float nrm = static_cast<float>(sqrt(tot));
-        if (!isfinite(nrm)) atomicOr(p.status, DMUON_DEV_NONFINITE_NORM);
-        p.s_norm[mat] = 1.0f / (nrm + p.eps);
-        p.counters[mat] = 0u;
-      }
-    }
-    __syncthreads();
+    __syncthreads();  // redd is reused by the next matrix
   }
 }
 
@@ -353,6 +354,11 @@ cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s) {
     momentum_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
   else
     momentum_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const StreamParams& p, int grid, cudaStream_t s) {
+  norm_finalize_kernel<<<grid, kStreamThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -38,8 +38,8 @@ FLAG_EPILOGUE_AX = 0x10
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 
-KIND_MOMENTUM, KIND_GRAM, KIND_POLY, KIND_GEMM, KIND_UPDATE0, KIND_SYMM = range(6)
-KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0", 5: "symm"}
+KIND_MOMENTUM, KIND_GRAM, KIND_POLY, KIND_GEMM, KIND_UPDATE0, KIND_SYMM, KIND_NORM = range(7)
+KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0", 5: "symm", 6: "norm"}
 
 # every symbol include/dmuon.h declares
 EXPORTS = (

@@ -110,9 +110,10 @@ def test_plan_buckets_tiles_and_work(name):
     assert sum(c["poly"] for c in d["lists"]) == g_tot
     assert sum(c["gemm"] for c in d["lists"]) == m_tot
     # launches per step and the algorithmic work the profiler attributes to them
-    assert len(d["launches"]) == 1 + 3 * w.ns_steps * d["chunks"]
+    assert len(d["launches"]) == 2 + 3 * w.ns_steps * d["chunks"]  # momentum, norm, 3 per step and chunk
     # every launch of a chunk shares the chunk's tile widths
-    for L in d["launches"][1:]:
+    assert [L["kind"] for L in d["launches"][:2]] == [dm.KIND_MOMENTUM, dm.KIND_NORM]
+    for L in d["launches"][2:]:
         assert L["bn"] in ((128, 256) if w.compute == "bf16" else (64,))
     work = {}
     for L in d["launches"]:
@@ -142,13 +143,13 @@ def test_many_buckets_split_into_chunks():
         groups[key] = groups.get(key, 0) + 1
     want = sum(cdiv(n, MAX_BUCKETS_PER_LAUNCH) for n in groups.values())
     assert len(groups) == 2 and d["chunks"] == want == 4
-    assert len(d["launches"]) == 1 + 3 * 2 * want
+    assert len(d["launches"]) == 2 + 3 * 2 * want
 
 
 def test_ns_steps_zero_plan():
     p = dm.dmuon_plan([(64, 128), (128, 64)], 0)
     kinds = [L["kind"] for L in p.describe()["launches"]]
-    assert kinds == [dm.KIND_MOMENTUM, dm.KIND_UPDATE0]
+    assert kinds == [dm.KIND_MOMENTUM, dm.KIND_NORM, dm.KIND_UPDATE0]
 
 
 def test_plan_is_deterministic():
@@ -166,7 +167,7 @@ def test_gram_form_plan_launches_and_work():
     forms = {(b["m"], b["n"]): b["form"] for b in d["buckets"]}
     assert forms == {(4096, 14336): "gram", (4096, 4096): "standard", (1024, 4096): "gram"}
     std_chunks, gram_chunks = 1, 1
-    assert len(d["launches"]) == 1 + 3 * S * std_chunks + (4 * S - 1) * gram_chunks
+    assert len(d["launches"]) == 2 + 3 * S * std_chunks + (4 * S - 1) * gram_chunks
     # executed work: standard buckets as before; Gram buckets: X X^T once, S polys, (S-1) Q products,
     # 2(S-1) G products (symmetric products counted once) and the final 2 m^2 n product
     want = 0.0
@@ -177,7 +178,7 @@ def test_gram_form_plan_launches_and_work():
             want += m * (m + 1) * n + S * sym + (S - 1) * sym + 2 * (S - 1) * sym + 2 * m * m * n
         else:
             want += wl.ns_flops(r, c, S)
-    got = sum(L["work"] for L in d["launches"] if L["kind"] != dm.KIND_MOMENTUM)
+    got = sum(L["work"] for L in d["launches"] if L["kind"] not in (dm.KIND_MOMENTUM, dm.KIND_NORM))
     assert abs(got - want) / want < 1e-12
     assert got < 0.6 * sum(wl.ns_flops(r, c, S) for r, c in w.shapes)
 
@@ -198,7 +199,7 @@ def test_polynomial_coefficients_per_launch(ax):
     coeffs = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.0, -1.5, 0.5)]
     p = dm.dmuon_plan([(256, 512), (512, 256)], 3, coeffs, flags=dm.FLAG_EPILOGUE_AX if ax else 0)
     launches = p.describe()["launches"]
-    for L in launches[1:]:
+    for L in launches[2:]:
         a, b, c = (float(np.float32(x)) for x in coeffs[L["step"]])
         if L["kind"] == dm.KIND_POLY:
             assert (L["b"], L["c"]) == pytest.approx((b, c), rel=1e-7)

@@ -242,7 +242,7 @@ def test_launch_count_per_step():
     assert d["chunks"] == 2
     c0 = run.muon.plan.launch_count()
     run.step()
-    assert run.muon.plan.launch_count() - c0 == len(d["launches"]) == 1 + 2 * 3 * 5
+    assert run.muon.plan.launch_count() - c0 == len(d["launches"]) == 2 + 2 * 3 * 5
 
 
 @pytest.mark.parametrize("flags", ["standard", "gram", "pair"])
