@@ -39,6 +39,7 @@ KERNEL_SOURCES = {
     "gram": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
     "poly": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
     "momentum": ["momentum.cu", "internal.h"],
+    "norm": ["momentum.cu", "internal.h"],
 }
 
 
