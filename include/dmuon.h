@@ -182,10 +182,14 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  *  nesterov         0 = heavy ball (U = M), 1 = Nesterov (U = G + mu*M).
  *
  * Each pointer must be 16-byte aligned and the matrices must not overlap.
- * The host pointer arrays are read during the call only. When the set of
- * pointers differs from the previous call's it is uploaded with a
- * cudaMemcpyAsync from host memory; under CUDA-graph capture, make one
- * uncaptured call with the same pointers first so that none is needed.
+ * The host pointer arrays are read during the call only. The plan keeps the
+ * last 4 distinct pointer sets resident on the device: a call whose pointers
+ * equal one of them copies nothing (alternating gradient buffers cost no
+ * copy after their first steps); otherwise the least recently used set is
+ * replaced by a cudaMemcpyAsync from host memory on `stream`. Under CUDA-graph
+ * capture, make one uncaptured call with the same pointers first so that none
+ * is needed; the captured graph stays valid while that pointer set remains
+ * one of the 4 resident ones.
  * Launches the momentum kernel and the per-matrix norm kernel, then
  * 3*ns_steps kernels per chunk of standard-form buckets and 4*ns_steps - 1
  * per chunk of Gram-space buckets (a chunk: up to 7 buckets sharing form and

@@ -53,6 +53,8 @@ constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+constexpr int kPtrSlots = 4;  // device-resident pointer tables per plan
+
 // Workspace buffers of a bucket, by role. Standard buckets use X0/X1 (the
 // iterate, ping-pong), A and B; Gram-space buckets use X0 (U, read twice), G,
 // P, Q0/Q1 (ping-pong) and R.
@@ -144,10 +146,16 @@ struct dmuon_plan_s {
   StreamParams sp{};
   std::vector<TcParams> tc_params;
   std::vector<SimtParams> simt_params;
-  uint64_t* host_ptrs = nullptr;  // pinned staging of the pointer table
-  std::vector<uint64_t> last_ptrs;
-  cudaEvent_t ptr_event = nullptr;
-  bool ptr_event_pending = false;
+  // Device-resident pointer tables (W, G, M device pointers per matrix), kPtrSlots of them, so
+  // that a step whose pointers match a resident table uploads nothing: alternating gradient
+  // buffers cost no copy after the first step with each. Each slot has its own pinned staging
+  // and an event that guards that staging until its upload has read it.
+  uint64_t* host_ptrs = nullptr;  // pinned staging, kPtrSlots tables
+  std::vector<uint64_t> slot_ptrs[kPtrSlots];
+  uint64_t slot_stamp[kPtrSlots] = {};
+  uint64_t ptr_clock = 0;
+  cudaEvent_t ptr_event[kPtrSlots] = {};
+  bool ptr_event_pending[kPtrSlots] = {};
   // ---- profiling
   bool prof = false;
   int32_t prof_max = 0, prof_n = 0;
@@ -372,7 +380,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   P.off_partial = take(4LL * std::max<int64_t>(units, 1));
   P.off_mats = take((int64_t)sizeof(MatDev) * n_mats);
   P.off_ub = take(8LL * (n_mats + 1));
-  P.off_ptrs = take(8LL * 3 * n_mats);
+  P.off_ptrs = take(8LL * 3 * n_mats * kPtrSlots);
   // tile lists: room for the longest lists any choice of tile widths gives (all 128 wide)
   int64_t cap_items = 0;
   if (P.ns_steps > 0) {
@@ -921,14 +929,18 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
     }
   }
 
-  // pinned staging for the per-step pointer table
+  // pinned staging for the per-step pointer tables
   if (P->host_ptrs == nullptr) {
-    if ((e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size())) != cudaSuccess)
+    if ((e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
       return cuda_fail(e, "cudaMallocHost");
-    if ((e = cudaEventCreateWithFlags(&P->ptr_event, cudaEventDisableTiming)) != cudaSuccess)
-      return cuda_fail(e, "cudaEventCreate");
+    for (int k = 0; k < kPtrSlots; ++k)
+      if ((e = cudaEventCreateWithFlags(&P->ptr_event[k], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreate");
   }
-  P->last_ptrs.clear();
+  for (int k = 0; k < kPtrSlots; ++k) {
+    P->slot_ptrs[k].clear();
+    P->slot_stamp[k] = 0;
+  }
   return DMUON_OK;
 }
 
@@ -958,24 +970,38 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     cur[2 * n + i] = m;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cur != P->last_ptrs) {
-    if (P->ptr_event_pending) {
-      if ((e = cudaEventSynchronize(P->ptr_event)) != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
-      P->ptr_event_pending = false;
+  // a resident table with these pointers, else refill the least recently used slot (the copy is
+  // ordered on the stream after every earlier step that may still read that slot)
+  int slot = -1;
+  for (int k = 0; k < kPtrSlots && slot < 0; ++k)
+    if (P->slot_ptrs[k] == cur) slot = k;
+  const size_t tab = cur.size();
+  if (slot < 0) {
+    slot = 0;
+    for (int k = 1; k < kPtrSlots; ++k)
+      if (P->slot_stamp[k] < P->slot_stamp[slot]) slot = k;
+    if (P->ptr_event_pending[slot]) {
+      if ((e = cudaEventSynchronize(P->ptr_event[slot])) != cudaSuccess)
+        return cuda_fail(e, "cudaEventSynchronize");
+      P->ptr_event_pending[slot] = false;
     }
-    std::memcpy(P->host_ptrs, cur.data(), 8 * cur.size());
-    if ((e = cudaMemcpyAsync(P->ws + P->off_ptrs, P->host_ptrs, 8 * cur.size(), cudaMemcpyHostToDevice, s)) !=
+    uint64_t* stage = P->host_ptrs + slot * tab;
+    std::memcpy(stage, cur.data(), 8 * tab);
+    if ((e = cudaMemcpyAsync(P->ws + P->off_ptrs + 8 * tab * slot, stage, 8 * tab, cudaMemcpyHostToDevice, s)) !=
         cudaSuccess)
       return cuda_fail(e, "pointer table upload");
-    if ((e = cudaEventRecord(P->ptr_event, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    P->ptr_event_pending = true;
-    P->last_ptrs = cur;
+    if ((e = cudaEventRecord(P->ptr_event[slot], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    P->ptr_event_pending[slot] = true;
+    P->slot_ptrs[slot] = std::move(cur);
   }
+  P->slot_stamp[slot] = ++P->ptr_clock;
+  const uint64_t* dptrs = reinterpret_cast<const uint64_t*>(P->ws + P->off_ptrs + 8 * tab * slot);
 
   StreamParams sp = P->sp;
   sp.mu = mu;
   sp.lr = lr;
   sp.nesterov = nesterov;
+  sp.ptrs = dptrs;
   for (const Launch& L : P->launches) {
     dmuon_status st = record_launch(*P, L, s, true);
     if (st != DMUON_OK) return st;
@@ -988,10 +1014,12 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     } else if (P->tc) {
       TcParams& tp = P->tc_params[L.param_index];
       tp.lr = lr;
+      tp.ptrs = dptrs;
       e = L.pair ? launch_tc_pair(L.phase, tp, L.grid, s) : launch_tc(L.phase, L.bn, tp, L.grid, s);
     } else {
       SimtParams& p = P->simt_params[L.param_index];
       p.lr = lr;
+      p.ptrs = dptrs;
       e = launch_simt(L.phase, p, L.grid, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -1169,9 +1197,11 @@ dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void
 void dmuon_plan_destroy(dmuon_plan_t P) {
   if (P == nullptr) return;
   destroy_events(*P);
-  if (P->ptr_event) {
-    cudaEventSynchronize(P->ptr_event);
-    cudaEventDestroy(P->ptr_event);
+  for (int k = 0; k < kPtrSlots; ++k) {
+    if (P->ptr_event[k]) {
+      cudaEventSynchronize(P->ptr_event[k]);
+      cudaEventDestroy(P->ptr_event[k]);
+    }
   }
   if (P->host_ptrs) cudaFreeHost(P->host_ptrs);
   delete P;

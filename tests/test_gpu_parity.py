@@ -245,6 +245,34 @@ def test_launch_count_per_step():
     assert run.muon.plan.launch_count() - c0 == len(d["launches"]) == 2 + 2 * 3 * 5
 
 
+def test_pointer_sets_resident_and_replaced():
+    """Steps that alternate among five gradient buffers (more than the four
+    pointer tables a plan keeps on the device, so tables are reused and
+    replaced) equal, bit for bit, steps that copy the same gradients into one
+    fixed buffer."""
+    shapes = [(300, 700), (700, 300), (256, 256)]
+    a = LibRun(shapes, capture=False)
+    b = LibRun(shapes, capture=False)
+    _fill(a, 7000, m_std=1e-3)
+    b.W.copy_(a.W)
+    b.M.copy_(a.M)
+    grads = []
+    for k in range(5):
+        g = torch.empty_like(a.G)
+        for i, (r, c) in enumerate(shapes):
+            o = a.offs[i]
+            g[o:o + r * c].copy_(random_matrix(r, c, 7100 + 10 * k + i, 1e-3, "cuda", "bf16").reshape(-1))
+        grads.append(g)
+    stream = torch.cuda.current_stream().cuda_stream
+    for k in [0, 1, 0, 1, 2, 3, 4, 0, 1, 2]:
+        a.muon.plan.step(a.ptrs(a.W), a.ptrs(grads[k]), a.ptrs(a.M), 0.02, 0.95, True, stream)
+        b.G.copy_(grads[k])
+        b.step()
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(a.W, b.W) and torch.equal(a.M, b.M)
+
+
 @pytest.mark.parametrize("flags", ["standard", "gram", "pair"])
 def test_cuda_graph_replay_matches_eager(flags):
     # after one uncaptured step with the same pointers, dmuon_step records no host copies and can be
