@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -80,11 +81,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(src: str) -> str:
+    """Source text without comments and blank space, so that the fingerprint
+    changes with the code and not with its comments."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_sha(kind: str) -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES.get(kind, []):
-        with open(os.path.join(ROOT, "matrix_optimizer_update_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "matrix_optimizer_update_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,12 +9,16 @@
 //                                Distributed Muon Training with Near-Adam
 //                                Overhead", gist.science summary section 2,
 //                                "Benutting van Symmetrie")
-//   poly:  B = b*A + c*(A A^T)  (A is symmetric, so A A = A A^T: the same
-//                                symmetric product on A, b*A added in the
-//                                epilogue from the same bf16 A tile)
-//   gemm:  X' = a*X + B X       (a*X added in the epilogue; on the last step
-//                                the epilogue applies W -= lr*scale*X' instead
-//                                of storing X')
+//   poly:  P = a*I + b*A + c*(A A^T)
+//                               (A is symmetric, so A A = A A^T: the same
+//                                symmetric product on A; b*A from the same
+//                                bf16 A tile and a on the diagonal are added
+//                                in the epilogue)
+//   gemm:  X' = P X = a*X + (b*A + c*A^2) X
+//                               (on the last step the epilogue applies
+//                                W -= lr*scale*X' instead of storing X'.
+//                                With DMUON_FLAG_EPILOGUE_AX the poly leaves
+//                                out a*I and the gemm epilogue adds a*X.)
 // At step 0 the Frobenius normalisation is folded in: the workspace holds the
 // unnormalised U and X0 = s*U with s = 1/(||U||_F + eps), so the gram epilogue
 // multiplies by s^2 and the gemm epilogue by s.
@@ -32,7 +36,11 @@
 // (two 128 x 256 fp32 accumulators) and one thread issues tcgen05.mma
 // (M=128, N=256, K=16); warps 2..9 drain an accumulator with tcgen05.ld
 // (two warps per TMEM lane quarter, one per column half) while the MMA warp
-// fills the other one. Every wait is bounded (see ptx.cuh).
+// fills the other one. The epilogue warps stage their 32 x 32 output chunks
+// in shared memory and write them with TMA stores (a symmetric chunk also as
+// its mirror image); on the last step they prefetch the weights' blocks with
+// cp.async and update them in shared memory. Every wait is bounded (see
+// ptx.cuh).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -48,9 +56,9 @@ constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 16 KB: 128 rows x 128 B
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
 constexpr int kStageBox = 32 * 32 * 2;            // one 32 x 32 bf16 box staged for a TMA store
 
-// Tile width N of one CTA (the UMMA N): 256, or 128 for buckets whose edges
-// would leave much of a 256-wide tile empty. Shared-memory stages fill the
-// same ~192 KB either way.
+// Tile width N of one CTA (the UMMA N): 256, or 128 where the planner's
+// tile-count cost favours it. Shared-memory stages fill the same 192 KB
+// either way; 32 KB of epilogue staging and 1 KB of barriers follow them.
 template <int BN>
 struct TcCfg {
   static constexpr uint32_t kStageB = BN * kTcBK * 2;  // BN rows x 128 B (or BN/64 x [64 k-rows x 128 B])

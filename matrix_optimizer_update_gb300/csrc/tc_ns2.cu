@@ -1,7 +1,9 @@
 // tc_ns2.cu - the Newton-Schulz products on CTA pairs: two-SM UMMA
 // (tcgen05 cta_group::2), 256 x 256 output tiles.
 //
-// Same phases and epilogues as tc_ns.cu (gram / poly / gemm, see there). A
+// Same phases as tc_ns.cu (gram / poly / gemm, see there); the epilogue is
+// the per-row form (epi::epilogue_chunk: each lane stores its own row, no
+// shared-memory staging, which the 6-stage ring leaves no room for). A
 // cluster of two CTAs on neighbouring SMs owns one tile: each CTA loads its
 // 128 rows of A and one half (128 rows, or 128 columns for the MN-major X
 // operand of the gemm) of B into its own shared memory, the leader CTA
