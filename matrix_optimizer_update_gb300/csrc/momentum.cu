@@ -73,6 +73,18 @@ __device__ __forceinline__ void store8_x(void* dst, int64_t e, const float (&u)[
   }
 }
 
+// 8 consecutive U values from the slot (bf16 or fp32), as fp32.
+__device__ __forceinline__ void load8_x(const char* X, int64_t e, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(X) + e);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+}
+
 template <bool GB>
 __device__ __forceinline__ float load1_grad(const void* g, int64_t e) {
   return GB ? __bfloat162float(reinterpret_cast<const bf16*>(g)[e]) : reinterpret_cast<const float*>(g)[e];
@@ -285,46 +297,114 @@ __global__ void __launch_bounds__(kStreamThreads) norm_finalize_kernel(const __g
   }
 }
 
-// ns_steps == 0: W -= lr * scale * s * U (U read back from the slot).
+// ns_steps == 0: W -= lr * scale * s * U (U read back from the slot), one
+// rounding into W, the same arithmetic per element on every path. Flat units
+// with bf16 weights and U move 8 elements per 16-byte access; tiles of
+// transposed matrices read U^T along its rows, turn it through shared memory
+// and update W rows 8 elements at a time; everything else goes element by
+// element.
+__device__ __forceinline__ float w_load(const void* W, bool wb, int64_t e) {
+  return wb ? __bfloat162float(reinterpret_cast<const bf16*>(W)[e]) : reinterpret_cast<const float*>(W)[e];
+}
+__device__ __forceinline__ void w_store(void* W, bool wb, int64_t e, float v) {
+  if (wb)
+    reinterpret_cast<bf16*>(W)[e] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(W)[e] = v;
+}
+
+// 8 consecutive bf16 weights w[e..e+7] -= f * x[0..7].
+__device__ __forceinline__ void w_update8_bf16(bf16* w, int64_t e, float f, const float (&x)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(w + e);
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 v = __bfloat1622float2(h[k]);
+    v.x -= f * x[2 * k];
+    v.y -= f * x[2 * k + 1];
+    h[k] = __floats2bfloat162_rn(v.x, v.y);
+  }
+  *reinterpret_cast<uint4*>(w + e) = u;
+}
+
 template <bool XB>
 __global__ void __launch_bounds__(kStreamThreads) update0_kernel(const __grid_constant__ StreamParams p) {
+  __shared__ float tileT[kTileC][kTileR + 1];  // U^T tile of a transposed matrix: [column][row]
   for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const int mat = find_matrix(p.unit_begin, p.n_mats, u);
     const MatDev md = p.mats[mat];
     const int64_t local = u - md.unit_begin;
-    const float f = p.lr * md.scale * p.s_norm[mat];
+    const float sn = p.s_norm[mat];
+    const float f = p.lr * md.scale * sn;
     const char* X = p.ws + md.x0_off;
     void* W = reinterpret_cast<void*>(p.ptrs[mat]);
-    int64_t e0, e1;
-    int r0 = 0, c0 = 0;
+    const bool wb = p.param_bf16 != 0;
+    float* cap = (p.capture != nullptr && md.cap_off >= 0) ? p.capture + md.cap_off : nullptr;
     if (md.flat) {
-      e0 = local * kFlatUnit;
-      e1 = min(e0 + kFlatUnit, (int64_t)md.rows * md.cols);
-    } else {
-      r0 = static_cast<int>(local / md.tiles_c) * kTileR;
-      c0 = static_cast<int>(local % md.tiles_c) * kTileC;
-      e0 = 0;
-      e1 = kTileR * kTileC;
-    }
-    for (int64_t q = e0 + threadIdx.x; q < e1; q += kStreamThreads) {
-      int64_t widx, xidx;
-      if (md.flat) {
-        widx = xidx = q;
+      const int64_t total = (int64_t)md.rows * md.cols;
+      const int64_t e0 = local * kFlatUnit, e1 = min(e0 + kFlatUnit, total);
+      if (XB && wb && e1 - e0 == kFlatUnit) {
+        constexpr int kV = kFlatUnit / (8 * kStreamThreads);
+#pragma unroll
+        for (int k = 0; k < kV; ++k) {
+          const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
+          float x[8];
+          load8_x(X, e, x);
+          w_update8_bf16(reinterpret_cast<bf16*>(W), e, f, x);
+          if (cap != nullptr)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) cap[e + q] = sn * x[q];
+        }
       } else {
-        const int r = r0 + static_cast<int>(q / kTileC), c = c0 + static_cast<int>(q % kTileC);
-        if (r >= md.rows || c >= md.cols) continue;
-        widx = (int64_t)r * md.cols + c;
-        xidx = md.transposed ? (int64_t)c * md.x_ld + r : (int64_t)r * md.x_ld + c;
+        for (int64_t q = e0 + threadIdx.x; q < e1; q += kStreamThreads) {
+          const float x = XB ? __bfloat162float(reinterpret_cast<const bf16*>(X)[q]) : reinterpret_cast<const float*>(X)[q];
+          w_store(W, wb, q, w_load(W, wb, q) - f * x);
+          if (cap != nullptr) cap[q] = sn * x;
+        }
       }
+      continue;
+    }
+    const int r0 = static_cast<int>(local / md.tiles_c) * kTileR;
+    const int c0 = static_cast<int>(local % md.tiles_c) * kTileC;
+    const bool full = r0 + kTileR <= md.rows && c0 + kTileC <= md.cols;
+    if (XB && wb && md.transposed && full && (md.cols & 7) == 0 && (md.x_ld & 7) == 0) {
+      // U^T rows c0..c0+127 (slot row pitch x_ld), 64 consecutive r each: 8 r per thread and vector
+#pragma unroll
+      for (int k = 0; k < (kTileC * kTileR / 8) / kStreamThreads; ++k) {
+        const int v = threadIdx.x + k * kStreamThreads;
+        const int cc = v / (kTileR / 8), rr = (v % (kTileR / 8)) * 8;
+        float x[8];
+        load8_x(X, (int64_t)(c0 + cc) * md.x_ld + r0 + rr, x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tileT[cc][rr + q] = x[q];
+      }
+      __syncthreads();
+      // W rows r0..r0+63, 8 consecutive columns per thread and vector
+#pragma unroll
+      for (int k = 0; k < (kTileR * kTileC / 8) / kStreamThreads; ++k) {
+        const int v = threadIdx.x + k * kStreamThreads;
+        const int rr = v / (kTileC / 8), cc = (v % (kTileC / 8)) * 8;
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = tileT[cc + q][rr];
+        const int64_t e = (int64_t)(r0 + rr) * md.cols + c0 + cc;
+        w_update8_bf16(reinterpret_cast<bf16*>(W), e, f, x);
+        if (cap != nullptr)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) cap[e + q] = sn * x[q];
+      }
+      __syncthreads();  // tileT is refilled by the next unit
+      continue;
+    }
+    for (int q = threadIdx.x; q < kTileR * kTileC; q += kStreamThreads) {
+      const int r = r0 + q / kTileC, c = c0 + q % kTileC;
+      if (r >= md.rows || c >= md.cols) continue;
+      const int64_t widx = (int64_t)r * md.cols + c;
+      const int64_t xidx = md.transposed ? (int64_t)c * md.x_ld + r : (int64_t)r * md.x_ld + c;
       const float x = XB ? __bfloat162float(reinterpret_cast<const bf16*>(X)[xidx])
                          : reinterpret_cast<const float*>(X)[xidx];
-      if (p.param_bf16) {
-        bf16* w = reinterpret_cast<bf16*>(W);
-        w[widx] = __float2bfloat16_rn(__bfloat162float(w[widx]) - f * x);
-      } else {
-        reinterpret_cast<float*>(W)[widx] -= f * x;
-      }
-      if (p.capture != nullptr && md.cap_off >= 0) p.capture[md.cap_off + widx] = p.s_norm[mat] * x;
+      w_store(W, wb, widx, w_load(W, wb, widx) - f * x);
+      if (cap != nullptr) cap[widx] = sn * x;
     }
   }
 }
