@@ -463,6 +463,7 @@ def run_ours(args):
                    "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
                    "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
+        "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
         "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
         "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
         "kernels": kernels, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
