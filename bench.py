@@ -150,14 +150,26 @@ class ClockSampler:
                     rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
                 except ValueError:
                     continue
+        note = None
         if not rows:
-            return None
+            # a timed region shorter than the sampling period: one reading right after it
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=30)
+                parts = [p.strip() for p in out.stdout.strip().splitlines()[0].split(",")]
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                note = "timed region shorter than the 200 ms sampling period: one reading taken right after it"
+            except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+                return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k, v in enumerate(r[3]) if v.lower() == "active"})
         loaded = [r for r in rows if r[2] > 300.0] or rows
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": max(r[2] for r in rows)}
+        clk = {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+               "reasons": reasons, "samples": 0 if note else len(rows), "samples_under_load": 0 if note else len(loaded),
+               "power_w_max": max(r[2] for r in rows)}
+        if note:
+            clk["note"] = note
+        return clk
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
