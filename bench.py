@@ -458,6 +458,36 @@ def run_ours(args):
                                        "d2h_bytes_per_step": hW.numel() * hW.element_size()}
         del hG, hW
 
+    # ---- optional: the AdamW kernel over the parameters Muon does not own (embedding, LM head and
+    # norms of Llama-3.1-8B: 2 x 128256 x 4096 + 65 x 4096 elements), bf16 params and grads, fp32 moments
+    adamw = None
+    if args.adamw:
+        n_aw = 2 * 128256 * 4096 + 65 * 4096
+        ap = torch.randn(n_aw, dtype=torch.bfloat16, device=f"cuda:{local}") * 0.02
+        ag = torch.randn(n_aw, dtype=torch.bfloat16, device=f"cuda:{local}") * 1e-3
+        am = torch.zeros(n_aw, dtype=torch.float32, device=f"cuda:{local}")
+        av = torch.zeros(n_aw, dtype=torch.float32, device=f"cuda:{local}")
+        torch.cuda.synchronize()
+
+        def aw_step(t):
+            dm.dmuon_adamw_flat(ap.data_ptr(), ag.data_ptr(), am.data_ptr(), av.data_ptr(), n_aw, "bf16", "bf16",
+                                lr=1e-3, step=t, stream=sh)
+
+        for t in range(1, args.warmup + 1):
+            aw_step(t)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for t in range(args.steps):
+            aw_step(args.warmup + 1 + t)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        aw_ms = a0.elapsed_time(a1) / args.steps
+        aw_bytes = n_aw * (2 + 2 + 2 + 8 + 8)  # p read + write, g read, m and v read + write
+        adamw = {"elements": n_aw, "ms_per_step": aw_ms, "gbs": aw_bytes / (aw_ms * 1e-3) / 1e9,
+                 "frac_of_hbm_peak": aw_bytes / (aw_ms * 1e-3) / 1e9 / hbm_peak,
+                 "bytes_per_element": 22, "launches_per_step": 1}
+        del ap, ag, am, av
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s, f, names = oracle_sample(w, args.cpu_budget)
@@ -479,6 +509,7 @@ def run_ours(args):
         "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
         "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
         "kernels": kernels, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
+        **({"adamw_other_params": adamw} if adamw is not None else {}),
         "gpu_launches": launches,
         "clocks": clk, "device_status": status,
     }
@@ -505,6 +536,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
     ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
+    ap.add_argument("--adamw", action="store_true",
+                    help="also time the AdamW kernel over Llama-3.1-8B's non-matrix parameters")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
     if args.impl == "reference":
