@@ -267,9 +267,8 @@ dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void
  * allocator already holds the whole GPU, a plugin handed only the tensors it
  * must update, or a runtime that forbids allocation in its steady state.
  * The pages have no counterpart; it is the plan-free form of the first
- * launch of dmuon_step, with its reduction scratch (per-tile partial sums
- * and a ticket counter) in a static device array of the library instead of
- * a workspace.
+ * launch of dmuon_step, with its reduction scratch (per-tile partial sums)
+ * in a static device array of the library instead of a workspace.
  *
  *  grad       device, rows x cols, grad_dtype (DMUON_F32 or DMUON_BF16), read only.
  *  momentum   device, rows x cols fp32, updated in place: M <- mu*M + G.
@@ -283,8 +282,11 @@ dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void
  * 256 B) stays allocated on every GPU that loads the library until the
  * process exits. The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. The call allocates nothing: it issues one
- * cudaMemsetAsync (clearing the ticket counter) and one kernel on stream.
+ * call before any stream capture. The call allocates nothing: it launches two
+ * kernels on stream (the tile pass, which writes one partial sum per tile,
+ * and a one-block kernel that adds them in a fixed order and writes s_out).
+ * 16-byte aligned grad, momentum and u_out (with cols % 4 == 0) take the
+ * vectorised path; other alignments are accepted and go element by element.
  * Every call shares the array and it keeps the last call's contents; calls
  * that overlap on the GPU race and give wrong results.
  */

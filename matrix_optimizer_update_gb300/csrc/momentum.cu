@@ -22,11 +22,15 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "stream_tile.cuh"
 
 namespace dmuon {
 namespace {
 
 using bf16 = __nv_bfloat16;
+using stile::load1_grad;
+using stile::store1_x;
+using stile::store8_x;
 
 __device__ __forceinline__ int find_matrix(const int64_t* unit_begin, int n_mats, int64_t u) {
   int lo = 0, hi = n_mats;  // unit_begin[lo] <= u < unit_begin[hi]
@@ -58,20 +62,6 @@ __device__ __forceinline__ void load8_grad(const void* g, int64_t e, float (&x)[
   }
 }
 
-template <bool XB>
-__device__ __forceinline__ void store8_x(void* dst, int64_t e, const float (&u)[8]) {
-  if (XB) {
-    uint4 o;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
-    *reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(dst) + e) = o;
-  } else {
-    float* d = reinterpret_cast<float*>(dst) + e;
-    *reinterpret_cast<float4*>(d) = make_float4(u[0], u[1], u[2], u[3]);
-    *reinterpret_cast<float4*>(d + 4) = make_float4(u[4], u[5], u[6], u[7]);
-  }
-}
 
 // 8 consecutive U values from the slot (bf16 or fp32), as fp32.
 __device__ __forceinline__ void load8_x(const char* X, int64_t e, float (&x)[8]) {
@@ -85,18 +75,7 @@ __device__ __forceinline__ void load8_x(const char* X, int64_t e, float (&x)[8])
   }
 }
 
-template <bool GB>
-__device__ __forceinline__ float load1_grad(const void* g, int64_t e) {
-  return GB ? __bfloat162float(reinterpret_cast<const bf16*>(g)[e]) : reinterpret_cast<const float*>(g)[e];
-}
 
-template <bool XB>
-__device__ __forceinline__ void store1_x(void* dst, int64_t e, float v) {
-  if (XB)
-    reinterpret_cast<bf16*>(dst)[e] = __float2bfloat16_rn(v);
-  else
-    reinterpret_cast<float*>(dst)[e] = v;
-}
 
 __device__ __forceinline__ float block_sum_f(float v, float* red) {
 #pragma unroll
@@ -180,94 +159,10 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
         }
       }
     } else {
-      const int tr = static_cast<int>(local / md.tiles_c), tc = static_cast<int>(local % md.tiles_c);
-      const int r0 = tr * kTileR, c0 = tc * kTileC;
-      // read 64 x 128 of G and M (4 consecutive columns per thread), update M, keep U in smem
-      const int cc = (threadIdx.x & 31) * 4;
-      if (md.vec_ok && r0 + kTileR <= md.rows && c0 + kTileC <= md.cols) {
-        // full tile: every load of the thread is issued before any store
-        constexpr int kP = kTileR / 8;
-        float g[kP][4];
-        float4 m4[kP];
-#pragma unroll
-        for (int pass = 0; pass < kP; ++pass) {
-          const int rr = pass * 8 + (threadIdx.x >> 5);
-          const int64_t e = (int64_t)(r0 + rr) * md.cols + c0 + cc;
-          if (GB) {
-            const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e));
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-            const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-            g[pass][0] = f0.x, g[pass][1] = f0.y, g[pass][2] = f1.x, g[pass][3] = f1.y;
-          } else {
-            const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e));
-            g[pass][0] = f.x, g[pass][1] = f.y, g[pass][2] = f.z, g[pass][3] = f.w;
-          }
-          m4[pass] = __ldcs(reinterpret_cast<const float4*>(M + e));
-        }
-#pragma unroll
-        for (int pass = 0; pass < kP; ++pass) {
-          const int rr = pass * 8 + (threadIdx.x >> 5);
-          const int64_t e = (int64_t)(r0 + rr) * md.cols + c0 + cc;
-          float mv[4] = {m4[pass].x, m4[pass].y, m4[pass].z, m4[pass].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            mv[q] = fmaf(mu, mv[q], g[pass][q]);
-            const float uu = nest ? fmaf(mu, mv[q], g[pass][q]) : mv[q];
-            ss = fmaf(uu, uu, ss);
-            tileU[rr][cc + q] = uu;
-          }
-          __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
-        }
-      } else {
-        for (int pass = 0; pass < kTileR / 8; ++pass) {
-          const int rr = pass * 8 + (threadIdx.x >> 5);
-          const int r = r0 + rr, c = c0 + cc;
-          float uu[4] = {0.f, 0.f, 0.f, 0.f};
-          if (r < md.rows) {
-            const int64_t e = (int64_t)r * md.cols + c;
-            for (int q = 0; q < 4 && c + q < md.cols; ++q) {
-              const float g = load1_grad<GB>(G, e + q);
-              const float mv = fmaf(mu, M[e + q], g);
-              M[e + q] = mv;
-              uu[q] = nest ? fmaf(mu, mv, g) : mv;
-              ss = fmaf(uu[q], uu[q], ss);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tileU[rr][cc + q] = uu[q];
-        }
-      }
+      const int r0 = static_cast<int>(local / md.tiles_c) * kTileR, c0 = static_cast<int>(local % md.tiles_c) * kTileC;
+      ss = stile::tile_update<GB>(G, M, md.rows, md.cols, md.vec_ok != 0, r0, c0, mu, nest, tileU);
       __syncthreads();
-      if (md.transposed) {
-        // U^T rows: slot element (c, r) at c*x_ld + r; 8 consecutive r per thread
-#pragma unroll
-        for (int pass = 0; pass < kTileC / 32; ++pass) {
-          const int jj = pass * 32 + (threadIdx.x >> 3);
-          const int ii = (threadIdx.x & 7) * 8;
-          const int c = c0 + jj, r = r0 + ii;
-          if (c >= md.cols) continue;
-          const int64_t e = (int64_t)c * md.x_ld + r;
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = tileU[ii + q][jj];
-          if (r + 8 <= md.rows) {
-            store8_x<XB>(X, e, v);
-          } else {
-            for (int q = 0; q < 8 && r + q < md.rows; ++q) store1_x<XB>(X, e + q, v[q]);
-          }
-        }
-      } else {
-        // same orientation, row pitch x_ld
-#pragma unroll 2
-        for (int pass = 0; pass < kTileR / 8; ++pass) {
-          const int rr = pass * 8 + (threadIdx.x >> 5);
-          const int cc = (threadIdx.x & 31) * 4;
-          const int r = r0 + rr, c = c0 + cc;
-          if (r >= md.rows) continue;
-          const int64_t e = (int64_t)r * md.x_ld + c;
-          for (int q = 0; q < 4 && c + q < md.cols; ++q) store1_x<XB>(X, e + q, tileU[rr][cc + q]);
-        }
-      }
+      stile::tile_store<XB>(X, md.x_ld, md.rows, md.cols, md.transposed != 0, true, r0, c0, tileU);
     }
 
     // the unit's partial sum of squares (the sum over the matrix is the finalize launch's)

@@ -10,9 +10,14 @@
 // static device array instead, so the caller passes only inputs and outputs.
 //
 // The array lives in every GPU that loads the library until the process
-// exits; it holds kNoallocMaxUnits fp32 partial sums plus one ticket counter
-// (256 KiB + 256 B). All calls share it: calls that overlap on the GPU (two
+// exits; it holds kNoallocMaxUnits fp32 partial sums (256 KiB, plus 256 B
+// kept free). All calls share it: calls that overlap on the GPU (two
 // streams, or two host threads) race on it and give wrong results.
+//
+// One call is two launches on the caller's stream: the tile pass (the same
+// 64 x 128 tile code as the workspace pass, stream_tile.cuh), where every
+// tile writes its partial sum of squares, then one CTA that adds the
+// partials in a fixed order in fp64 and writes s.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -21,6 +26,7 @@
 
 #include "dmuon.h"
 #include "internal.h"
+#include "stream_tile.cuh"
 
 namespace dmuon {
 namespace {
@@ -28,10 +34,9 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kNoallocMaxUnits = 65536;  // 64 x 128 tiles per matrix
-constexpr int kNoallocCounterSlot = kNoallocMaxUnits;  // the ticket counter sits after the partials
 constexpr int kNoallocWords = kNoallocMaxUnits + 64;
 
-// Static scratch: [0, kNoallocMaxUnits) fp32 partial sums (as raw words), then the ticket counter.
+// Static scratch: [0, kNoallocMaxUnits) fp32 partial sums, stored as raw words.
 static __device__ __align__(256) unsigned g_noalloc_scratch[kNoallocWords];
 
 struct NoallocParams {
@@ -43,58 +48,24 @@ struct NoallocParams {
   int32_t rows, cols, u_ld, tiles_c;
   int32_t n_tiles;
   int32_t transposed;
+  int32_t vec_load, vec_store;  // 16-byte access allowed (alignment of the pointers, cols % 4)
   float mu, eps;
   int32_t nesterov;
 };
 
 template <bool GB, bool XB>
-__global__ void __launch_bounds__(kStreamThreads) momentum_norm_noalloc_kernel(const __grid_constant__ NoallocParams p) {
+__global__ void __launch_bounds__(kStreamThreads) momentum_noalloc_kernel(const __grid_constant__ NoallocParams p) {
   __shared__ float tileU[kTileR][kTileC + 1];
   __shared__ float red[kStreamThreads / 32];
-  __shared__ double redd[kStreamThreads / 32];
-  __shared__ int is_last;
   float* partial = reinterpret_cast<float*>(p.scratch);
-  unsigned* counter = p.scratch + kNoallocCounterSlot;
   const bool nest = p.nesterov != 0;
-
   for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
     const int r0 = (t / p.tiles_c) * kTileR, c0 = (t % p.tiles_c) * kTileC;
-    float ss = 0.f;
-    for (int e = threadIdx.x; e < kTileR * kTileC; e += kStreamThreads) {
-      const int rr = e / kTileC, cc = e % kTileC;
-      const int r = r0 + rr, c = c0 + cc;
-      float u = 0.f;
-      if (r < p.rows && c < p.cols) {
-        const int64_t idx = (int64_t)r * p.cols + c;
-        const float g = GB ? __bfloat162float(reinterpret_cast<const bf16*>(p.grad)[idx])
-                           : reinterpret_cast<const float*>(p.grad)[idx];
-        const float mv = fmaf(p.mu, p.momentum[idx], g);
-        p.momentum[idx] = mv;
-        u = nest ? fmaf(p.mu, mv, g) : mv;
-        ss = fmaf(u, u, ss);
-      }
-      tileU[rr][cc] = u;
-    }
+    float ss = stile::tile_update<GB>(p.grad, p.momentum, p.rows, p.cols, p.vec_load != 0, r0, c0, p.mu, nest,
+                                      tileU);
     __syncthreads();
-    for (int e = threadIdx.x; e < kTileR * kTileC; e += kStreamThreads) {
-      // write in the short-side orientation: (r, c) as is, or (c, r) when rows > cols
-      int rr, cc;
-      if (p.transposed) {
-        cc = e / kTileR;
-        rr = e % kTileR;
-      } else {
-        rr = e / kTileC;
-        cc = e % kTileC;
-      }
-      const int r = r0 + rr, c = c0 + cc;
-      if (r >= p.rows || c >= p.cols) continue;
-      const int64_t o = p.transposed ? (int64_t)c * p.u_ld + r : (int64_t)r * p.u_ld + c;
-      if (XB)
-        reinterpret_cast<bf16*>(p.u)[o] = __float2bfloat16_rn(tileU[rr][cc]);
-      else
-        reinterpret_cast<float*>(p.u)[o] = tileU[rr][cc];
-    }
-    // per-tile partial, fixed-order block sum
+    stile::tile_store<XB>(p.u, p.u_ld, p.rows, p.cols, p.transposed != 0, p.vec_store != 0, r0, c0, tileU);
+    // the tile's partial, fixed-order block sum
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -103,26 +74,25 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_norm_noalloc_kernel(c
       float b = 0.f;
       for (int k = 0; k < kStreamThreads / 32; ++k) b += red[k];
       partial[t] = b;
-      __threadfence();
-      is_last = (atomicAdd(counter, 1u) == static_cast<unsigned>(p.n_tiles - 1));
     }
-    __syncthreads();
-    if (is_last) {
-      __threadfence();
-      double acc = 0.0;
-      for (int k = threadIdx.x; k < p.n_tiles; k += kStreamThreads) acc += (double)__ldcg(&partial[k]);
+    __syncthreads();  // tileU and red are reused by the next tile
+  }
+}
+
+// s = 1 / (||U||_F + eps) from the tiles' partials, in fp64 and a fixed order.
+__global__ void __launch_bounds__(kStreamThreads) noalloc_finalize_kernel(const __grid_constant__ NoallocParams p) {
+  __shared__ double redd[kStreamThreads / 32];
+  const float* partial = reinterpret_cast<const float*>(p.scratch);
+  double acc = 0.0;
+  for (int k = threadIdx.x; k < p.n_tiles; k += kStreamThreads) acc += static_cast<double>(partial[k]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = acc;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        double tot = 0.0;
-        for (int k = 0; k < kStreamThreads / 32; ++k) tot += redd[k];
-        *p.s_out = 1.0f / (static_cast<float>(sqrt(tot)) + p.eps);
-        *counter = 0u;  // leave the ticket at zero for the next call
-      }
-    }
-    __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int k = 0; k < kStreamThreads / 32; ++k) tot += redd[k];
+    *p.s_out = 1.0f / (static_cast<float>(sqrt(tot)) + p.eps);
   }
 }
 
@@ -171,9 +141,6 @@ extern "C" dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* mom
     scratch = g_scratch_addr[dev];
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the ticket counter must start at zero, whatever an earlier call left behind
-  if (cudaMemsetAsync(scratch + kNoallocCounterSlot, 0, sizeof(unsigned), s) != cudaSuccess)
-    return set_last_error(DMUON_ERR_CUDA, "cudaMemsetAsync of the ticket counter failed");
 
   NoallocParams p;
   p.grad = grad;
@@ -191,18 +158,23 @@ extern "C" dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* mom
   p.mu = mu;
   p.eps = eps;
   p.nesterov = nesterov;
+  const auto aligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
+  p.vec_load = (cols % 4 == 0) && aligned(momentum, 16) && aligned(grad, grad_dtype == DMUON_BF16 ? 8 : 16);
+  p.vec_store = aligned(u_out, 16);
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = static_cast<int>(std::min<int64_t>(n_tiles, 4LL * (sms > 0 ? sms : 1)));
   const bool gb = grad_dtype == DMUON_BF16, xb = u_dtype == DMUON_BF16;
   if (gb && xb)
-    momentum_norm_noalloc_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(p);
+    momentum_noalloc_kernel<true, true><<<grid, kStreamThreads, 0, s>>>(p);
   else if (gb)
-    momentum_norm_noalloc_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(p);
+    momentum_noalloc_kernel<true, false><<<grid, kStreamThreads, 0, s>>>(p);
   else if (xb)
-    momentum_norm_noalloc_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
+    momentum_noalloc_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
   else
-    momentum_norm_noalloc_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
+    momentum_noalloc_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "kernel launch failed");
+  noalloc_finalize_kernel<<<1, kStreamThreads, 0, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "kernel launch failed");
   return set_last_error(DMUON_OK, "");
 }
