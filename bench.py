@@ -39,8 +39,8 @@ KERNEL_SOURCES = {
     "gemm": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
     "gram": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
     "poly": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
-    "momentum": ["momentum.cu", "internal.h"],
-    "norm": ["momentum.cu", "internal.h"],
+    "momentum": ["momentum.cu", "stream_tile.cuh", "internal.h"],
+    "norm": ["momentum.cu", "stream_tile.cuh", "internal.h"],
 }
 
 
