@@ -91,8 +91,8 @@ typedef struct {
                                           Space Recurrence"). Fewer flops when the
                                           matrix is wide (>= 26% fewer at 2:1);
                                           others keep the standard form.          */
-#define DMUON_FLAG_PAIR_TILES 0x8u    /* buckets whose short side is >= 256 and
-                                          whose products run 256 wide use
+#define DMUON_FLAG_PAIR_TILES 0x8u    /* buckets whose short side is a multiple
+                                          of 256 and whose products run 256 wide use
                                           256 x 256 tiles on pairs of SMs
                                           (two-SM UMMA, thread-block clusters of
                                           2). bf16 only.                        */

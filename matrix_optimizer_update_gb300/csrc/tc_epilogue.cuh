@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dmuon {
 namespace epi {
@@ -391,6 +392,142 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
       }
     }
   }
+}
+
+// ---- the per-tile epilogue of one epilogue warp, shared by the one-SM and
+// the two-SM kernels. The warp owns 32 accumulator rows (its TMEM lane
+// quarter) and kChunks 32-column chunks of them: output rows i0 + lane,
+// columns jbase + 32 ch (tbase: the chunks' TMEM address). wait_acc() waits
+// for the accumulator (false when the CTA gave up). Before that wait the
+// operands that do not depend on the accumulator are fetched: the linear
+// term's first two chunks, and on the last step the first two W blocks. Then
+// each chunk is drained and written: through a staged TMA box (X', symmetric
+// chunks above the diagonal, with the mirror image), through the staged W
+// update, or per row (diagonal chunks, matrix edges, fp32 weights, a*X in
+// the epilogue). stg: this warp's two staging boxes; nbox counts the X' boxes
+// (their double buffering spans tiles).
+constexpr int kStageBox = 32 * 32 * 2;  // one 32 x 32 bf16 box staged for a TMA store
+
+template <int PHASE, int kChunks, class WaitAcc>
+__device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket& B, const int4& it, int i0, int jbase,
+                                              uint32_t tbase, int lane, uint8_t* stg, uint32_t& nbox,
+                                              WaitAcc&& wait_acc) {
+  const int i = i0 + lane;
+  // The linear term's operand does not depend on the accumulator: the first
+  // two chunks are fetched while the MMAs of this tile are still running,
+  // each later chunk while the chunk two places before it is processed.
+  // Poly (b*A): the chunk's 32 x 32 block of A, coalesced (lane: row
+  // (lane >> 2) + 8u, 16-byte piece lane & 3), only where the chunk touches
+  // the upper triangle. Gemm with a*X in the epilogue: this lane's row.
+  const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
+  const bf16* abase = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride);
+  const bf16* row = abase + (int64_t)i * B.aux_ld;
+  // gemm with a == 0 (the last product of the Gram-space recurrence) has no linear term
+  const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
+  uint4 cur[4], nxt[4];
+  auto fetch = [&](int ch, uint4 (&dst)[4]) {
+    const int j0 = jbase + ch * 32;
+    if (PHASE == kPhasePoly) {
+      if (j0 + 32 <= B.m && j0 + 31 >= i0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ii = i0 + (lane >> 2) + 8 * u;
+          if (ii < B.m)
+            dst[u] = __ldg(reinterpret_cast<const uint4*>(abase + (int64_t)ii * B.aux_ld + j0 + 8 * (lane & 3)));
+        }
+      }
+    } else if (need_aux && i < B.m && j0 + 32 <= lim) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
+    }
+  };
+  fetch(0, cur);
+  fetch(1, nxt);
+  const int gm = B.slot_mat[it.y];
+  const MatDev md = p.mats[gm];
+  // last step on bf16 weights: the W blocks of the first two chunks are copied in while the
+  // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
+  const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
+  if (w_last) {
+    w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase, lane, stg);
+    ptx::cp_async_commit();
+    w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase + 32, lane, stg + kStageBox);
+    ptx::cp_async_commit();
+  }
+  if (!wait_acc()) return false;
+  ptx::tc_fence_after();
+  float sc = 1.f;
+  if (p.first) {
+    const float s = p.s_norm[gm];
+    sc = (PHASE == kPhaseGram) ? s * s : s;
+  }
+  // Output chunks leave through shared memory and TMA stores (one 32 x 32 box per chunk, and
+  // its mirror image for the symmetric products): X' of the gemm (not on the last step, which
+  // updates W, nor when a*X is added here), and every chunk of a symmetric product strictly
+  // above the diagonal. On the last step bf16 weights are updated in shared memory from
+  // prefetched blocks. Diagonal chunks, matrix edges and fp32 weights take the per-row path.
+  const bool gemm_tma = PHASE == kPhaseGemm && !p.last && !need_aux;
+#pragma unroll 1
+  for (int ch = 0; ch < kChunks; ++ch) {
+    float v[32];
+    ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
+    const int j0 = jbase + ch * 32;
+    if (PHASE == kPhaseGemm && gemm_tma) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] *= sc;
+      uint8_t* box = stg + (nbox & 1u) * kStageBox;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this box is done with it
+      __syncwarp();
+      stage_row_sw64(box, lane, v);
+      ptx::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (i0 < B.m && j0 < B.n) ptx::tma_store_3d(&B.tmOut, box, j0, i0, it.y);
+        ptx::bulk_commit();  // one group per box, stored or not, so the count above holds
+      }
+      ++nbox;
+    } else if (PHASE == kPhaseGemm && w_last) {
+      uint8_t* box = stg + (ch & 1) * kStageBox;
+      ptx::cp_async_wait<1>();  // this chunk's copies (all but the newest group) have landed
+      __syncwarp();
+      if (w_chunk_vec(md, B.m, B.n, i0, j0)) {
+        gemm_values(p, B, it.y, i, j0, sc, v, cur);
+        capture_row(p, md, i, j0, B.m, B.n, v);
+        w_chunk_apply(p, md, gm, B.m, B.n, i0, j0, lane, v, box);
+      } else {
+        epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);  // matrix edges
+      }
+      if (ch + 2 < kChunks) w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
+      ptx::cp_async_commit();
+    } else if (PHASE != kPhaseGemm && i0 < B.m && j0 < B.m && j0 + 31 >= i0) {
+      // a chunk of a symmetric product touching the upper triangle
+      if (lane == 0) ptx::bulk_wait_read<0>();  // both boxes free again
+      __syncwarp();
+      float a[32];
+      if (PHASE == kPhasePoly) poly_aux_rows(B, abase, i, j0, lane, cur, stg, a);
+      if (j0 >= i0 + 32) {  // strictly above the diagonal: the chunk and its mirror as TMA boxes
+        sym_values<PHASE>(p, sc, a, v);
+        stage_row_sw64(stg, lane, v);
+        stage_col_sw64(stg + kStageBox, lane, v);
+        ptx::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(&B.tmOut, stg, j0, i0, it.y);
+          ptx::tma_store_3d(&B.tmOut, stg + kStageBox, i0, j0, it.y);
+          ptx::bulk_commit();
+        }
+      } else {  // on the diagonal: per-row stores keep the result exactly symmetric
+        sym_diag_chunk<PHASE>(p, B, it.y, i, j0, sc, a, v);
+      }
+    } else if (PHASE == kPhaseGemm) {
+      epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+    if (ch + 2 < kChunks) fetch(ch + 2, nxt);
+  }
+  return true;
 }
 
 }  // namespace epi

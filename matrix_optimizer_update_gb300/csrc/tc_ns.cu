@@ -54,7 +54,7 @@ using bf16 = __nv_bfloat16;
 
 constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 16 KB: 128 rows x 128 B
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
-constexpr int kStageBox = 32 * 32 * 2;            // one 32 x 32 bf16 box staged for a TMA store
+using epi::kStageBox;
 
 // Tile width N of one CTA (the UMMA N): 256, or 128 where the planner's
 // tile-count cost favours it. Shared-memory stages fill the same 192 KB
@@ -227,123 +227,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
       const int i0 = it.z * kTcBM + q * 32;
-      const int i = i0 + lane;
       const int jbase = it.w * BN + half * (BN / 2);
-      // The linear term's operand does not depend on the accumulator: the first
-      // two chunks are fetched while the MMAs of this tile are still running,
-      // each later chunk while the chunk two places before it is processed.
-      // Poly (b*A): the chunk's 32 x 32 block of A, coalesced (lane: row
-      // (lane >> 2) + 8u, 16-byte piece lane & 3), only where the chunk touches
-      // the upper triangle. Gemm with a*X in the epilogue: this lane's row.
-      const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
-      const bf16* abase = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride);
-      const bf16* row = abase + (int64_t)i * B.aux_ld;
-      // gemm with a == 0 (the last product of the Gram-space recurrence) has no linear term
-      const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
-      uint4 cur[4], nxt[4];
-      auto fetch = [&](int ch, uint4 (&dst)[4]) {
-        const int j0 = jbase + ch * 32;
-        if (PHASE == kPhasePoly) {
-          if (j0 + 32 <= B.m && j0 + 31 >= i0) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int ii = i0 + (lane >> 2) + 8 * u;
-              if (ii < B.m)
-                dst[u] = __ldg(reinterpret_cast<const uint4*>(abase + (int64_t)ii * B.aux_ld + j0 + 8 * (lane & 3)));
-            }
-          }
-        } else if (need_aux && i < B.m && j0 + 32 <= lim) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
-        }
-      };
-      fetch(0, cur);
-      fetch(1, nxt);
-      const int gm = B.slot_mat[it.y];
-      const MatDev md = p.mats[gm];
-      // last step on bf16 weights: the W blocks of the first two chunks are copied in while the
-      // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
-      const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
-      if (w_last) {
-        epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase, lane, stg);
-        ptx::cp_async_commit();
-        epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase + 32, lane, stg + kStageBox);
-        ptx::cp_async_commit();
-      }
-      if (!ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
-      ptx::tc_fence_after();
-      float sc = 1.f;
-      if (p.first) {
-        const float s = p.s_norm[gm];
-        sc = (PHASE == kPhaseGram) ? s * s : s;
-      }
       const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
-      // Output chunks leave through shared memory and TMA stores (one 32 x 32 box per chunk, and
-      // its mirror image for the symmetric products): X' of the gemm (not on the last step, which
-      // updates W, nor when a*X is added here), and every chunk of a symmetric product strictly
-      // above the diagonal. On the last step bf16 weights are updated in shared memory from
-      // prefetched blocks. Diagonal chunks, matrix edges and fp32 weights take the per-row path.
-      const bool gemm_tma = PHASE == kPhaseGemm && !p.last && !need_aux;
-#pragma unroll 1
-      for (int ch = 0; ch < kEpiChunks; ++ch) {
-        float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
-        const int j0 = jbase + ch * 32;
-        if (PHASE == kPhaseGemm && gemm_tma) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= sc;
-          uint8_t* box = stg + (nbox & 1u) * kStageBox;
-          if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this box is done with it
-          __syncwarp();
-          epi::stage_row_sw64(box, lane, v);
-          ptx::fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            if (i0 < B.m && j0 < B.n) ptx::tma_store_3d(&B.tmOut, box, j0, i0, it.y);
-            ptx::bulk_commit();  // one group per box, stored or not, so the count above holds
-          }
-          ++nbox;
-        } else if (PHASE == kPhaseGemm && w_last) {
-          uint8_t* box = stg + (ch & 1) * kStageBox;
-          ptx::cp_async_wait<1>();  // this chunk's copies (all but the newest group) have landed
-          __syncwarp();
-          if (epi::w_chunk_vec(md, B.m, B.n, i0, j0)) {
-            epi::gemm_values(p, B, it.y, i, j0, sc, v, cur);
-            epi::capture_row(p, md, i, j0, B.m, B.n, v);
-            epi::w_chunk_apply(p, md, gm, B.m, B.n, i0, j0, lane, v, box);
-          } else {
-            epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);  // matrix edges
-          }
-          if (ch + 2 < kEpiChunks) epi::w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
-          ptx::cp_async_commit();
-        } else if (PHASE != kPhaseGemm && i0 < B.m && j0 < B.m && j0 + 31 >= i0) {
-          // a chunk of a symmetric product touching the upper triangle
-          if (lane == 0) ptx::bulk_wait_read<0>();  // both boxes free again
-          __syncwarp();
-          float a[32];
-          if (PHASE == kPhasePoly) epi::poly_aux_rows(B, abase, i, j0, lane, cur, stg, a);
-          if (j0 >= i0 + 32) {  // strictly above the diagonal: the chunk and its mirror as TMA boxes
-            epi::sym_values<PHASE>(p, sc, a, v);
-            epi::stage_row_sw64(stg, lane, v);
-            epi::stage_col_sw64(stg + kStageBox, lane, v);
-            ptx::fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_3d(&B.tmOut, stg, j0, i0, it.y);
-              ptx::tma_store_3d(&B.tmOut, stg + kStageBox, i0, j0, it.y);
-              ptx::bulk_commit();
-            }
-          } else {  // on the diagonal: per-row stores keep the result exactly symmetric
-            epi::sym_diag_chunk<PHASE>(p, B, it.y, i, j0, sc, a, v);
-          }
-        } else if (PHASE == kPhaseGemm) {
-          epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
-        if (ch + 2 < kEpiChunks) fetch(ch + 2, nxt);
-      }
+      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
+        return ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);
+      });
+      if (!ok) break;
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->tempty[acc]);

@@ -1,9 +1,9 @@
 // tc_ns2.cu - the Newton-Schulz products on CTA pairs: two-SM UMMA
 // (tcgen05 cta_group::2), 256 x 256 output tiles.
 //
-// Same phases as tc_ns.cu (gram / poly / gemm, see there); the epilogue is
-// the per-row form (epi::epilogue_chunk: each lane stores its own row, no
-// shared-memory staging, which the 6-stage ring leaves no room for). A
+// Same phases and the same per-tile epilogue as tc_ns.cu (gram / poly /
+// gemm, epi::epilogue_tile: TMA-stored output boxes, prefetched W blocks on
+// the last step). A
 // cluster of two CTAs on neighbouring SMs owns one tile: each CTA loads its
 // 128 rows of A and one half (128 rows, or 128 columns for the MN-major X
 // operand of the gemm) of B into its own shared memory, the leader CTA
@@ -53,6 +53,8 @@ struct PairShared {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(PairShared) <= 1024, "barriers must fit their 1 KB");
+using epi::kStageBox;
 
 template <int PHASE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_constant__ TcParams p) {
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
   uint8_t* sA = base;
   uint8_t* sB = base + kStages * kHalfA;
   PairShared* sh = reinterpret_cast<PairShared*>(sB + kStages * kHalfB);
+  // epilogue staging: two 2 KB boxes per epilogue warp, after the barriers' 1 KB
+  uint8_t* stg_all = sB + kStages * kHalfB + 1024;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
   const int warp = threadIdx.x >> 5;
@@ -188,50 +192,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t lead_tempty = ptx::mapa_shared(ptx::smem_u32(&sh->tempty[0]), 0);
-    uint32_t local = 0;
+    uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
+    uint32_t local = 0, nbox = 0;
     for (int w = pair; w < p.n_items; w += npairs, ++local) {
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
-      const int i = it.z * kPairBM + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const int i0 = it.z * kPairBM + static_cast<int>(rank) * 128 + q * 32;
       const int jbase = it.w * kPairBN + half * (kPairBN / 2);
-      const int lim = (PHASE == kPhasePoly) ? B.m : B.n;
-      const bf16* row = reinterpret_cast<const bf16*>(B.aux + it.y * B.aux_mat_stride) + (int64_t)i * B.aux_ld;
-      const bool need_aux = PHASE == kPhasePoly || (PHASE == kPhaseGemm && p.a != 0.f);
-      uint4 cur[4], nxt[4];
-      auto fetch = [&](int ch, uint4 (&dst)[4]) {
-        const int j0 = jbase + ch * 32;
-        if (need_aux && i < B.m && j0 + 32 <= lim) {
-          const uint4* s4 = reinterpret_cast<const uint4*>(row + j0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) dst[u] = __ldg(s4 + u);
-        }
-      };
-      fetch(0, cur);
-      fetch(1, nxt);
-      if (!ptx::mbar_wait_cluster(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns)) break;
-      ptx::tc_fence_after();
-      const int gm = B.slot_mat[it.y];
-      const MatDev md = p.mats[gm];
-      float sc = 1.f;
-      if (p.first) {
-        const float s = p.s_norm[gm];
-        sc = (PHASE == kPhaseGram) ? s * s : s;
-      }
       const uint32_t tbase = tmem + acc * kPairBN + half * (kPairBN / 2) + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int ch = 0; ch < kEpiChunks; ++ch) {
-        float v[32];
-        ptx::tmem_ld_32x32b_x32(tbase + ch * 32, v);
-        epi::epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, jbase + ch * 32, sc, v, cur);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
-        if (ch + 2 < kEpiChunks) fetch(ch + 2, nxt);
-      }
+      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
+        return ptx::mbar_wait_cluster(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);
+      });
+      if (!ok) break;
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(lead_tempty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
     }
+    if (lane == 0) ptx::bulk_wait_all();  // every TMA store of this warp has landed
+    ptx::cp_async_wait<0>();              // and every W copy (matters only after an abort)
   }
 
   __syncthreads();
@@ -245,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
 
 template <int PHASE>
 cudaError_t launch_pair_phase(const TcParams& p, int pairs, cudaStream_t s) {
-  const size_t smem = 1024 + kStages * (kHalfA + kHalfB) + sizeof(PairShared);
+  const size_t smem = 1024 + kStages * (kHalfA + kHalfB) + 1024 + kEpiWarps * kStageBox * 2;
   cudaError_t e = cudaFuncSetAttribute(tc_ns_pair_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -10,7 +10,10 @@ from test_gpu_parity import _check_all, _fill
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(300, 700), (700, 300), (520, 1000), (256, 1536), (1536, 256), (512, 512), (384, 384), (130, 130)]
+# pair buckets: short side a multiple of 256 (512 x 1000 and 1000 x 512 with ragged long sides);
+# the others run on one-SM tiles beside them
+SHAPES = [(300, 700), (700, 300), (520, 1000), (256, 1536), (1536, 256), (512, 512), (384, 384), (130, 130),
+          (512, 1000), (1000, 512)]
 
 
 def test_pair_tiles_small():
@@ -28,7 +31,8 @@ def test_pair_tiles_small():
 def test_pair_tiles_ragged(gram):
     run = LibRun(SHAPES, pair=True, gram_ns=gram)
     pairs = {(b["m"], b["n"]): b["pair"] for b in run.muon.plan.describe()["buckets"]}
-    assert pairs[(512, 512)] and pairs[(256, 1536)] and not pairs[(300, 700)] and not pairs[(130, 130)]
+    assert pairs[(512, 512)] and pairs[(256, 1536)] and pairs[(512, 1000)]
+    assert not pairs[(300, 700)] and not pairs[(130, 130)] and not pairs[(520, 1000)] and not pairs[(384, 384)]
     init = _fill(run, 5100, m_std=1e-3)
     run.step()
     torch.cuda.synchronize()
