@@ -377,7 +377,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   };
   P.off_status = take(256);
   P.off_s = take(4LL * n_mats);
-  P.off_partial = take(4LL * std::max<int64_t>(units, 1));
+  P.off_partial = take(4LL * kPartialsPerUnit * std::max<int64_t>(units, 1));
   P.off_mats = take((int64_t)sizeof(MatDev) * n_mats);
   P.off_ub = take(8LL * (n_mats + 1));
   P.off_ptrs = take(8LL * 3 * n_mats * kPtrSlots);
@@ -434,7 +434,7 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   P.launches.push_back(L);
   Launch nf;
   nf.kind = DMUON_KIND_NORM;
-  nf.work = 4.0 * static_cast<double>(P.n_units) + 4.0 * n_mats;  // partials read, s written
+  nf.work = 4.0 * kPartialsPerUnit * static_cast<double>(P.n_units) + 4.0 * n_mats;  // partials read, s written
   P.launches.push_back(nf);
   if (P.ns_steps == 0) {
     Launch u;

@@ -31,6 +31,7 @@ constexpr int kFlatUnit = 8192;
 constexpr int kTileR = 64;
 constexpr int kTileC = 128;
 constexpr int kStreamThreads = 256;
+constexpr int kPartialsPerUnit = kStreamThreads / 32;  // one sum of squares per warp and unit
 
 enum Phase : int { kPhaseGram = 1, kPhasePoly = 2, kPhaseGemm = 3 };
 
@@ -57,7 +58,7 @@ struct StreamParams {
   const int64_t* unit_begin;  // [n_mats + 1]
   const uint64_t* ptrs;       // [3 * n_mats]: W, G, M device pointers
   char* ws;
-  float* partial;             // [n_units]: each unit's sum of squares of U
+  float* partial;             // [n_units * kPartialsPerUnit]: per warp and unit, sums of squares of U
   float* s_norm;              // [n_mats]: 1 / (||U||_F + eps)
   unsigned* status;
   float* capture;

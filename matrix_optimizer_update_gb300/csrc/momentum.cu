@@ -77,17 +77,6 @@ __device__ __forceinline__ void load8_x(const char* X, int64_t e, float (&x)[8])
 
 
 
-__device__ __forceinline__ float block_sum_f(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x == 0)
-    for (int k = 0; k < kStreamThreads / 32; ++k) t += red[k];
-  return t;  // valid in thread 0
-}
 
 __device__ __forceinline__ double block_sum_d(double v, double* red) {
 #pragma unroll
@@ -104,7 +93,6 @@ __device__ __forceinline__ double block_sum_d(double v, double* red) {
 template <bool GB, bool XB>
 __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_constant__ StreamParams p) {
   __shared__ float tileU[kTileR][kTileC + 1];
-  __shared__ float redf[kStreamThreads / 32];
   const float mu = p.mu;
   const bool nest = p.nesterov != 0;
 
@@ -165,10 +153,12 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
       stile::tile_store<XB>(X, md.x_ld, md.rows, md.cols, md.transposed != 0, true, r0, c0, tileU);
     }
 
-    // the unit's partial sum of squares (the sum over the matrix is the finalize launch's)
-    const float bs = block_sum_f(ss, redf);
-    if (threadIdx.x == 0) p.partial[u] = bs;
-    __syncthreads();  // redf is reused by the next unit
+    // the unit's partial sums of squares, one per warp (the sum over the matrix is the finalize
+    // launch's): no barrier between units
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) p.partial[u * kPartialsPerUnit + (threadIdx.x >> 5)] = ss;
+    if (!md.flat) __syncthreads();  // tileU is refilled by the next unit
   }
 }
 
@@ -180,8 +170,8 @@ __global__ void __launch_bounds__(kStreamThreads) norm_finalize_kernel(const __g
   for (int mat = blockIdx.x; mat < p.n_mats; mat += gridDim.x) {
     const MatDev md = p.mats[mat];
     double acc = 0.0;
-    for (int64_t k = threadIdx.x; k < md.unit_count; k += kStreamThreads)
-      acc += static_cast<double>(p.partial[md.unit_begin + k]);
+    for (int64_t k = threadIdx.x; k < md.unit_count * kPartialsPerUnit; k += kStreamThreads)
+      acc += static_cast<double>(p.partial[md.unit_begin * kPartialsPerUnit + k]);
     const double tot = block_sum_d(acc, redd);
     if (threadIdx.x == 0) {
       const float nrm = static_cast<float>(sqrt(tot));
