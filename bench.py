@@ -25,6 +25,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -119,7 +120,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dmuon_bench_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -176,9 +177,9 @@ class ClockSampler:
 class HostBuffer:
     """Page-locked host memory for the end-to-end copies: torch's pinned
     allocation, or anonymous memory advised to use transparent huge pages and
-    registered with the CUDA driver (use_thp). Which is faster differs from box
-    to box: measured host-device rates ranged from 28 to 211 GB/s for either
-    kind, depending on the box and on what ran on it before."""
+    registered with the CUDA driver (use_thp). Which is faster differs from one
+    machine to another: measured host-device rates ranged from 28 to 211 GB/s for either
+    kind, depending on the machine and on what ran on it before."""
 
     def __init__(self, like, use_thp: bool):
         import mmap
@@ -514,7 +515,7 @@ def run_ours(args):
                "result_read": "device status word (dmuon_read_device_status), every step",
                "timing": "host wall clock from the first upload to the last status read",
                "overlap": "next step's gradient upload overlaps the current step (two device buffers)",
-               "host_memory": f"{hbG.kind} (the faster of two kinds on this box: {hbG.rate_gbs:.0f} GB/s to the device)",
+               "host_memory": f"{hbG.kind} (the faster of two kinds on this machine: {hbG.rate_gbs:.0f} GB/s to the device)",
                "device_status": bits}
         del gbuf[1]
         hbW = fastest_host_buffer(ms.W, to_device=False)  # reads W, leaves it as it is
