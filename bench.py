@@ -274,6 +274,18 @@ def oracle_sample(workload, budget_s: float, start_layer: int = 0, max_mats=None
     return spent, done_flops, names
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return "unknown"
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -306,7 +318,9 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "matrices": len(w.shapes), "sample_per_step": names},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"per step: {', '.join(names)} (fp64 numpy oracle, whole matrices)"},
+                         "sample": f"per step: {', '.join(names)} (fp64 numpy oracle, whole matrices)",
+                         "cpu_model": cpu_model(),
+                         "extrapolated_step_ms": wl.totals(w)["ns_flops"] / (value * 1e12) * 1e3},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -576,7 +590,9 @@ def run_ours(args):
         s, f, names = oracle_sample(w, args.cpu_budget)
         cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{len(names)} whole matrices of layer 0 in order ({'; '.join(names)}), fp64 numpy, "
-                         f"{s:.1f} s"}
+                         f"{s:.1f} s",
+               "cpu_model": cpu_model(),
+               "extrapolated_step_ms": tot["ns_flops"] / (f / s) * 1e3}
 
     value = aggregate(tot["ns_flops"], args.steps, world, max_ms * 1e-3)
     line = {
