@@ -60,3 +60,25 @@ def test_pair_tiles_deterministic():
     run.M.copy_(M0)
     run.step()
     assert torch.equal(run.W, W1) and torch.equal(run.M, M1)
+
+
+def test_pair_tiles_with_ax_epilogue():
+    """Pair tiles with the literal form of the step (a*X read in the last product's epilogue)."""
+    run = LibRun([(512, 1000), (1000, 512), (256, 768)], pair=True, epilogue_ax=True)
+    assert all(b["pair"] for b in run.muon.plan.describe()["buckets"])
+    init = _fill(run, 5400, m_std=1e-3)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    _check_all(run, init)
+
+
+@pytest.mark.parametrize("param,grad", [("f32", "bf16"), ("bf16", "f32")])
+def test_pair_tiles_mixed_storage(param, grad):
+    """Pair tiles with fp32 weights (the per-row weight update) or fp32 gradients."""
+    run = LibRun([(256, 512), (512, 256), (512, 1000)], param=param, grad=grad, compute="bf16", pair=True)
+    init = _fill(run, 5500, m_std=1e-3)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    _check_all(run, init)
