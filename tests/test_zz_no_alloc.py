@@ -22,25 +22,26 @@ from helpers import TOL_M, TOL_X, LibRun, rel
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("shape", [(300, 700), (700, 300), (1024, 4096)])
-def test_noalloc_pass_matches_dmuon_step_twice(shape):
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(300, 700), (700, 300), (1024, 4096), (129, 257)])
+def test_noalloc_pass_matches_dmuon_step_twice(shape, dtype):
     r, c = shape
     m, n = min(r, c), max(r, c)
     u_ld = (n + 7) // 8 * 8
     stream = torch.cuda.current_stream().cuda_stream
-    run = LibRun([shape], param="bf16", grad="bf16", compute="bf16", ns_steps=0)
+    run = LibRun([shape], param=dtype, grad=dtype, compute=dtype, ns_steps=0)
     M0 = random_matrix(r, c, 4100, 1e-3, "cuda", "f32")
     run.set(0, M=M0)
     M_na = M0.clone()
-    u = torch.empty(m, u_ld, dtype=torch.bfloat16, device="cuda")
+    u = torch.empty(m, u_ld, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32, device="cuda")
     s = torch.empty(1, dtype=torch.float32, device="cuda")
     for call in range(2):
-        G = random_matrix(r, c, 4200 + call, 1e-3, "cuda", "bf16")
+        G = random_matrix(r, c, 4200 + call, 1e-3, "cuda", dtype)
         run.set(0, G=G)
         run.step(lr=0.02, mu=0.95, nesterov=True)
         x_step = run.update(0).double().cpu().numpy()  # s * U in W's orientation
         dm.dmuon_momentum_norm_noalloc(G.data_ptr(), M_na.data_ptr(), u.data_ptr(), s.data_ptr(), r, c,
-                                       "bf16", "bf16", 0.95, True, 1e-7, stream)
+                                       dtype, dtype, 0.95, True, 1e-7, stream)
         torch.cuda.synchronize()
         U = u[:, :n].double()
         if r > c:
