@@ -46,8 +46,8 @@ EXPORTS = (
     "dmuon_plan", "dmuon_plan_workspace_bytes", "dmuon_plan_bind", "dmuon_step",
     "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
     "dmuon_profile_begin", "dmuon_profile_end", "dmuon_plan_costs", "dmuon_launch_count",
-    "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_assign_owners", "dmuon_adamw_flat", "dmuon_plan_destroy",
-    "dmuon_last_error", "dmuon_version",
+    "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_assign_owners", "dmuon_adamw_flat",
+    "dmuon_plan_destroy", "dmuon_last_error", "dmuon_version",
 )
 
 
