@@ -82,3 +82,21 @@ def test_pair_tiles_mixed_storage(param, grad):
     torch.cuda.synchronize()
     assert run.status() == 0
     _check_all(run, init)
+
+
+@pytest.mark.parametrize("gram", [False, True])
+def test_pair_and_one_sm_tiles_agree_bitwise(gram):
+    """Two-SM and one-SM tiles sum every output element over K in the same order: the stored weights
+    and momenta of both plans are identical, bit for bit."""
+    shapes = [(512, 1024), (1024, 512), (256, 768)]
+    a = LibRun(shapes, pair=False, gram_ns=gram, capture=False)
+    b = LibRun(shapes, pair=True, gram_ns=gram, capture=False)
+    assert all(x["pair"] for x in b.muon.plan.describe()["buckets"])
+    _fill(a, 5600, m_std=1e-3)
+    b.W.copy_(a.W)
+    b.G.copy_(a.G)
+    b.M.copy_(a.M)
+    a.step()
+    b.step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.W, b.W) and torch.equal(a.M, b.M)
