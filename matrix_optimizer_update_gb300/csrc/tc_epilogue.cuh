@@ -160,11 +160,12 @@ __device__ __forceinline__ void sym_diag_chunk(const TcParams& p, const TcBucket
 // ---- last step on bf16 weights: W -= lr * scale * X, one 32 x 32 chunk of X
 // (rows i0.., columns j0.. in the iteration's orientation) at a time. The
 // chunk's W block is copied into shared memory ahead of time (cp.async, 16
-// bytes per lane and row segment), updated there row by row from the fp32 X
-// each lane holds (one rounding per element), and written back with
-// coalesced 16-byte stores. Box layout: 32 rows of 64 bytes, piece c of row
-// r at piece c ^ ((r >> 1) & 3). Box rows are W rows: i0 + r for W = m x n,
-// j0 + r for W = n x m (stored transposed).
+// bytes per lane and row segment), updated there from the fp32 X each lane
+// holds (one rounding per element), and written back by the bulk-copy engine,
+// one 64-byte copy per W row, so the warp does not wait on the stores. Box
+// layout: 32 rows of 64 bytes in order (a row is one contiguous copy). Box
+// rows are W rows: i0 + r for W = m x n, j0 + r for W = n x m (stored
+// transposed).
 
 // Whole chunk inside W with 16-byte aligned row segments (else the per-row path).
 __device__ __forceinline__ bool w_chunk_vec(const MatDev& md, int m, int n, int i0, int j0) {
@@ -177,9 +178,7 @@ __device__ __forceinline__ int64_t w_seg(const MatDev& md, int m, int n, int i0,
   return (i0 + rr < m) ? (int64_t)(i0 + rr) * n + j0 + 8 * pc : -1;
 }
 
-__device__ __forceinline__ uint8_t* box_piece(uint8_t* box, int r, int c) {
-  return box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-}
+__device__ __forceinline__ uint8_t* box_piece(uint8_t* box, int r, int c) { return box + r * 64 + (c << 4); }
 
 __device__ __forceinline__ void w_chunk_fetch(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
                                               int j0, int lane, uint8_t* box) {
@@ -194,7 +193,9 @@ __device__ __forceinline__ void w_chunk_fetch(const TcParams& p, const MatDev& m
   }
 }
 
-// The copies of this chunk must have landed (cp_async_wait + __syncwarp) before the call.
+// The copies of this chunk must have landed (cp_async_wait + __syncwarp) before
+// the call. Leaves one bulk group per lane (its row's copy back to W); the box
+// is free again once every lane's group has read it (bulk_wait_read + __syncwarp).
 __device__ __forceinline__ void w_chunk_apply(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
                                               int j0, int lane, const float (&v)[32], uint8_t* box) {
   const float step = p.lr * md.scale;
@@ -220,16 +221,12 @@ __device__ __forceinline__ void w_chunk_apply(const TcParams& p, const MatDev& m
       *e = __float2bfloat16_rn(__bfloat162float(*e) - step * v[k]);
     }
   }
+  ptx::fence_proxy_async_shared();
   __syncwarp();
   bf16* W = reinterpret_cast<bf16*>(p.ptrs[gm]);
-  const int pc = lane & 3;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int rr = (lane >> 2) + 8 * u;
-    const int64_t off = w_seg(md, m, n, i0, j0, rr, pc);
-    if (off >= 0) *reinterpret_cast<uint4*>(W + off) = *reinterpret_cast<const uint4*>(box_piece(box, rr, pc));
-  }
-  __syncwarp();
+  const int64_t off = w_seg(md, m, n, i0, j0, lane, 0);
+  if (off >= 0) ptx::bulk_store(W + off, box_piece(box, lane, 0), 64);
+  ptx::bulk_commit();
 }
 
 // The linear term and the normalisation of the last product's chunk: v = (a x + v) s.
@@ -450,6 +447,8 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket&
   // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
   const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
   if (w_last) {
+    ptx::bulk_wait_read<0>();  // the previous tile's copies back to W are done with both boxes
+    __syncwarp();
     w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase, lane, stg);
     ptx::cp_async_commit();
     w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase + 32, lane, stg + kStageBox);
@@ -498,7 +497,11 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket&
       } else {
         epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);  // matrix edges
       }
-      if (ch + 2 < kChunks) w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
+      if (ch + 2 < kChunks) {
+        ptx::bulk_wait_read<0>();  // this chunk's rows have left the box
+        __syncwarp();
+        w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
+      }
       ptx::cp_async_commit();
     } else if (PHASE != kPhaseGemm && i0 < B.m && j0 < B.m && j0 + 31 >= i0) {
       // a chunk of a symmetric product touching the upper triangle

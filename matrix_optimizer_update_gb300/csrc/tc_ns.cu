@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sh->tempty[acc]);
     }
-    if (lane == 0) ptx::bulk_wait_all();  // every TMA store of this warp has landed
-    ptx::cp_async_wait<0>();              // and every W copy (matters only after an abort)
+    ptx::bulk_wait_all();      // every bulk store of this warp (TMA boxes, W rows) has landed
+    ptx::cp_async_wait<0>();   // and every W copy (matters only after an abort)
   }
 
   __syncthreads();

@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(lead_tempty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
     }
-    if (lane == 0) ptx::bulk_wait_all();  // every TMA store of this warp has landed
-    ptx::cp_async_wait<0>();              // and every W copy (matters only after an abort)
+    ptx::bulk_wait_all();      // every bulk store of this warp (TMA boxes, W rows) has landed
+    ptx::cp_async_wait<0>();   // and every W copy (matters only after an abort)
   }
 
   __syncthreads();
