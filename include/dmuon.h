@@ -186,7 +186,11 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  * last 4 distinct pointer sets resident on the device: a call whose pointers
  * equal one of them copies nothing (alternating gradient buffers cost no
  * copy after their first steps); otherwise the least recently used set is
- * replaced by a cudaMemcpyAsync from host memory on `stream`. Under CUDA-graph
+ * replaced by a cudaMemcpyAsync from host memory on `stream`. With bf16
+ * weights on the tensor-core path a resident set also holds a TMA tensor map
+ * of every W (encoded on the host when the set is first seen, copied with the
+ * pointers): the last Newton-Schulz product stores its updated W boxes
+ * through them. Under CUDA-graph
  * capture, make one uncaptured call with the same pointers first so that none
  * is needed; the captured graph stays valid while that pointer set remains
  * one of the 4 resident ones.

@@ -137,7 +137,7 @@ struct dmuon_plan_s {
   // ---- workspace layout (byte offsets)
   size_t ws_bytes = 0;
   int64_t off_status = 0, off_s = 0, off_partial = 0, off_mats = 0, off_ub = 0, off_ptrs = 0,
-          off_items = 0, off_probe = 0, off_capture = -1;
+          off_items = 0, off_probe = 0, off_capture = -1, off_wmaps = -1;
   int64_t cap_elems = 0;
   // ---- binding
   char* ws = nullptr;
@@ -151,6 +151,9 @@ struct dmuon_plan_s {
   // buffers cost no copy after the first step with each. Each slot has its own pinned staging
   // and an event that guards that staging until its upload has read it.
   uint64_t* host_ptrs = nullptr;  // pinned staging, kPtrSlots tables
+  // With each resident pointer set, a TMA map of every W (tensor-core path, bf16 weights): the
+  // last step's epilogue stores its updated W boxes through them. Pinned staging per slot.
+  CUtensorMap* host_wmaps = nullptr;
   std::vector<uint64_t> slot_ptrs[kPtrSlots];
   uint64_t slot_stamp[kPtrSlots] = {};
   uint64_t ptr_clock = 0;
@@ -381,6 +384,8 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   P.off_mats = take((int64_t)sizeof(MatDev) * n_mats);
   P.off_ub = take(8LL * (n_mats + 1));
   P.off_ptrs = take(8LL * 3 * n_mats * kPtrSlots);
+  if (P.tc && P.dt.param == DMUON_BF16 && P.ns_steps > 0)
+    P.off_wmaps = take((int64_t)sizeof(CUtensorMap) * n_mats * kPtrSlots);
   // tile lists: room for the longest lists any choice of tile widths gives (all 128 wide)
   int64_t cap_items = 0;
   if (P.ns_steps > 0) {
@@ -520,6 +525,25 @@ dmuon_status make_map(CUtensorMap* map, const void* base, int inner, int rows, i
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DMUON_OK;
+}
+
+// W (rows x cols bf16, row-major) as a 2-D map of 32 x 32 boxes with the 64-byte swizzle, for
+// the TMA stores of the last step's W update. All zeros when the row pitch is not a multiple of
+// 16 bytes: the kernels then update that W row by row and never use the map.
+dmuon_status make_wmap(CUtensorMap* map, const void* W, int rows, int cols) {
+  std::memset(map, 0, sizeof(CUtensorMap));
+  if (cols % 8 != 0) return DMUON_OK;
+  auto enc = get_encode_fn();
+  if (enc == nullptr) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix (%d)", (int)r);
   return DMUON_OK;
 }
 
@@ -933,6 +957,9 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   if (P->host_ptrs == nullptr) {
     if ((e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
       return cuda_fail(e, "cudaMallocHost");
+    if (P->off_wmaps >= 0 &&
+        (e = cudaMallocHost(&P->host_wmaps, sizeof(CUtensorMap) * P->mats.size() * kPtrSlots)) != cudaSuccess)
+      return cuda_fail(e, "cudaMallocHost");
     for (int k = 0; k < kPtrSlots; ++k)
       if ((e = cudaEventCreateWithFlags(&P->ptr_event[k], cudaEventDisableTiming)) != cudaSuccess)
         return cuda_fail(e, "cudaEventCreate");
@@ -985,6 +1012,17 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
         return cuda_fail(e, "cudaEventSynchronize");
       P->ptr_event_pending[slot] = false;
     }
+    P->slot_ptrs[slot].clear();  // holds no valid set until both uploads below are queued
+    if (P->off_wmaps >= 0) {
+      CUtensorMap* wst = P->host_wmaps + slot * n;
+      for (size_t i = 0; i < n; ++i) {
+        dmuon_status st = make_wmap(wst + i, params[i], P->mats[i].rows, P->mats[i].cols);
+        if (st != DMUON_OK) return st;
+      }
+      if ((e = cudaMemcpyAsync(P->ws + P->off_wmaps + sizeof(CUtensorMap) * n * slot, wst, sizeof(CUtensorMap) * n,
+                               cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "weight tensor-map upload");
+    }
     uint64_t* stage = P->host_ptrs + slot * tab;
     std::memcpy(stage, cur.data(), 8 * tab);
     if ((e = cudaMemcpyAsync(P->ws + P->off_ptrs + 8 * tab * slot, stage, 8 * tab, cudaMemcpyHostToDevice, s)) !=
@@ -996,6 +1034,9 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
   }
   P->slot_stamp[slot] = ++P->ptr_clock;
   const uint64_t* dptrs = reinterpret_cast<const uint64_t*>(P->ws + P->off_ptrs + 8 * tab * slot);
+  const CUtensorMap* dwmaps =
+      P->off_wmaps >= 0 ? reinterpret_cast<const CUtensorMap*>(P->ws + P->off_wmaps + sizeof(CUtensorMap) * n * slot)
+                        : nullptr;
 
   StreamParams sp = P->sp;
   sp.mu = mu;
@@ -1015,6 +1056,7 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
       TcParams& tp = P->tc_params[L.param_index];
       tp.lr = lr;
       tp.ptrs = dptrs;
+      tp.wmaps = dwmaps;
       e = L.pair ? launch_tc_pair(L.phase, tp, L.grid, s) : launch_tc(L.phase, L.bn, tp, L.grid, s);
     } else {
       SimtParams& p = P->simt_params[L.param_index];
@@ -1204,6 +1246,7 @@ void dmuon_plan_destroy(dmuon_plan_t P) {
     }
   }
   if (P->host_ptrs) cudaFreeHost(P->host_ptrs);
+  if (P->host_wmaps) cudaFreeHost(P->host_wmaps);
   delete P;
 }
 

@@ -93,6 +93,7 @@ struct TcParams {
   float diag;  // poly phase: added on the diagonal (a*I of the Gram-space polynomial)
   const MatDev* mats;
   const uint64_t* ptrs;
+  const CUtensorMap* wmaps;  // last step on bf16 weights: per matrix, W as 32 x 32 boxes (64-byte swizzle)
   const float* s_norm;
   float* capture;
   unsigned* status;

@@ -161,11 +161,12 @@ __device__ __forceinline__ void sym_diag_chunk(const TcParams& p, const TcBucket
 // (rows i0.., columns j0.. in the iteration's orientation) at a time. The
 // chunk's W block is copied into shared memory ahead of time (cp.async, 16
 // bytes per lane and row segment), updated there from the fp32 X each lane
-// holds (one rounding per element), and written back by the bulk-copy engine,
-// one 64-byte copy per W row, so the warp does not wait on the stores. Box
-// layout: 32 rows of 64 bytes in order (a row is one contiguous copy). Box
-// rows are W rows: i0 + r for W = m x n, j0 + r for W = n x m (stored
-// transposed).
+// holds (one rounding per element), and written back by one TMA store of the
+// box through the matrix's own tensor map (p.wmaps), so the warp does not wait
+// on the stores and the TMA unit sees one operation per chunk. Box layout: 32
+// rows of 64 bytes, piece c of row r at piece c ^ ((r >> 1) & 3) (the 64-byte
+// swizzle of the map). Box rows are W rows: i0 + r for W = m x n, j0 + r for
+// W = n x m (stored transposed).
 
 // Whole chunk inside W with 16-byte aligned row segments (else the per-row path).
 __device__ __forceinline__ bool w_chunk_vec(const MatDev& md, int m, int n, int i0, int j0) {
@@ -178,7 +179,9 @@ __device__ __forceinline__ int64_t w_seg(const MatDev& md, int m, int n, int i0,
   return (i0 + rr < m) ? (int64_t)(i0 + rr) * n + j0 + 8 * pc : -1;
 }
 
-__device__ __forceinline__ uint8_t* box_piece(uint8_t* box, int r, int c) { return box + r * 64 + (c << 4); }
+__device__ __forceinline__ uint8_t* box_piece(uint8_t* box, int r, int c) {
+  return box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
 
 __device__ __forceinline__ void w_chunk_fetch(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
                                               int j0, int lane, uint8_t* box) {
@@ -194,8 +197,8 @@ __device__ __forceinline__ void w_chunk_fetch(const TcParams& p, const MatDev& m
 }
 
 // The copies of this chunk must have landed (cp_async_wait + __syncwarp) before
-// the call. Leaves one bulk group per lane (its row's copy back to W); the box
-// is free again once every lane's group has read it (bulk_wait_read + __syncwarp).
+// the call. Lane 0 commits one bulk group (the box's store to W); the box is
+// free again once that group has read it (lane 0 bulk_wait_read + __syncwarp).
 __device__ __forceinline__ void w_chunk_apply(const TcParams& p, const MatDev& md, int gm, int m, int n, int i0,
                                               int j0, int lane, const float (&v)[32], uint8_t* box) {
   const float step = p.lr * md.scale;
@@ -223,10 +226,11 @@ __device__ __forceinline__ void w_chunk_apply(const TcParams& p, const MatDev& m
   }
   ptx::fence_proxy_async_shared();
   __syncwarp();
-  bf16* W = reinterpret_cast<bf16*>(p.ptrs[gm]);
-  const int64_t off = w_seg(md, m, n, i0, j0, lane, 0);
-  if (off >= 0) ptx::bulk_store(W + off, box_piece(box, lane, 0), 64);
-  ptx::bulk_commit();
+  if (lane == 0) {  // W rows past the matrix's edge are clipped by the map
+    if (md.transposed) ptx::tma_store_2d(&p.wmaps[gm], box, i0, j0);
+    else ptx::tma_store_2d(&p.wmaps[gm], box, j0, i0);
+    ptx::bulk_commit();
+  }
 }
 
 // The linear term and the normalisation of the last product's chunk: v = (a x + v) s.
@@ -445,9 +449,12 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket&
   const MatDev md = p.mats[gm];
   // last step on bf16 weights: the W blocks of the first two chunks are copied in while the
   // MMAs still run; chunk ch + 2's while chunk ch is processed (one copy group per chunk)
-  const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16;
+  const bool w_last = PHASE == kPhaseGemm && p.last && p.param_bf16 && p.wmaps != nullptr;
   if (w_last) {
-    ptx::bulk_wait_read<0>();  // the previous tile's copies back to W are done with both boxes
+    if (lane == 0) {
+      ptx::bulk_wait_read<0>();  // the previous tile's stores to W are done with both boxes
+      ptx::fence_tensormap_acquire(&p.wmaps[gm]);
+    }
     __syncwarp();
     w_chunk_fetch(p, md, gm, B.m, B.n, i0, jbase, lane, stg);
     ptx::cp_async_commit();
@@ -498,7 +505,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket&
         epilogue_chunk<PHASE>(p, B, md, gm, it.y, i, j0, sc, v, cur);  // matrix edges
       }
       if (ch + 2 < kChunks) {
-        ptx::bulk_wait_read<0>();  // this chunk's rows have left the box
+        if (lane == 0) ptx::bulk_wait_read<0>();  // this chunk's store has read the box
         __syncwarp();
         w_chunk_fetch(p, md, gm, B.m, B.n, i0, j0 + 64, lane, box);
       }

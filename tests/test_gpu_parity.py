@@ -276,21 +276,20 @@ def test_pointer_sets_resident_and_replaced():
 def test_weight_sets_replaced_store_through_their_own_maps():
     """Six weight/momentum replicas stepped in turn through one plan. That is
     more pointer sets than the four a plan keeps on the device, so slots are
-    refilled with the tensor maps of other weight buffers. Each replica must
-    equal, bit for bit, the same steps run through one fixed buffer. Every
-    buffer stays allocated: a map left over from another set would write into
-    a live buffer and show up here as a mismatch."""
+    refilled with the tensor maps of other weight buffers. Each replica's
+    matrices must equal, bit for bit, the same steps run through one fixed
+    buffer. Every buffer stays allocated: a map left over from another set
+    would write into a live buffer and show up here as a mismatch."""
     shapes = [(520, 1000), (1000, 520), (256, 256)]  # row pitches of 16-byte multiples: box stores
     a = LibRun(shapes, capture=False)
     b = LibRun(shapes, capture=False)
     _fill(a, 7300, m_std=1e-3)
     Ws, Ms = [], []
     for k in range(6):
-        W, M = torch.empty_like(a.W), torch.empty_like(a.M)
+        W, M = torch.zeros_like(a.W), torch.zeros_like(a.M)
         for i, (r, c) in enumerate(shapes):
-            o = a.offs[i]
-            W[o:o + r * c].copy_(random_matrix(r, c, 7400 + 10 * k + i, 0.02, "cuda", "bf16").reshape(-1))
-            M[o:o + r * c].copy_(random_matrix(r, c, 7500 + 10 * k + i, 1e-3, "cuda", "f32").reshape(-1))
+            a.view(W, i).copy_(random_matrix(r, c, 7400 + 10 * k + i, 0.02, "cuda", "bf16"))
+            a.view(M, i).copy_(random_matrix(r, c, 7500 + 10 * k + i, 1e-3, "cuda", "f32"))
         Ws.append(W)
         Ms.append(M)
     Wb, Mb = [w.clone() for w in Ws], [m.clone() for m in Ms]
@@ -306,7 +305,9 @@ def test_weight_sets_replaced_store_through_their_own_maps():
     torch.cuda.synchronize()
     assert a.status() == 0 and b.status() == 0
     for k in range(6):
-        assert torch.equal(Ws[k], Wb[k]) and torch.equal(Ms[k], Mb[k]), k
+        for i in range(len(shapes)):
+            assert torch.equal(a.view(Ws[k], i), a.view(Wb[k], i)), (k, i)
+            assert torch.equal(a.view(Ms[k], i), a.view(Mb[k], i)), (k, i)
 
 
 @pytest.mark.parametrize("flags", ["standard", "gram", "pair"])
