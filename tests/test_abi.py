@@ -126,6 +126,23 @@ def test_plan_buckets_tiles_and_work(name):
     assert p.workspace_bytes() > 0
 
 
+def test_workspace_holds_weight_maps_only_where_the_last_step_stores_through_them():
+    """With bf16 weights on the tensor-core path, the workspace holds a
+    128-byte TMA map of every weight matrix for each of the four resident
+    pointer sets (the last step stores its updated W boxes through them).
+    fp32 weights, fp32 compute and ns_steps = 0 need none."""
+    shapes = [(520, 1000), (1000, 520), (256, 256), (4096, 1024), (3000, 100)]
+    align = 1024  # workspace regions start on 1024-byte boundaries
+
+    def ws(ns_steps=5, **kw):
+        return dm.dmuon_plan(shapes, ns_steps, **kw).workspace_bytes()
+
+    grow = ws(param="bf16") - ws(param="f32")
+    assert 4 * len(shapes) * 128 <= grow < 4 * len(shapes) * 128 + align
+    assert ws(param="bf16", compute="f32") == ws(param="f32", compute="f32")
+    assert ws(0, param="bf16") == ws(0, param="f32")
+
+
 MAX_BUCKETS_PER_LAUNCH = 7
 
 
