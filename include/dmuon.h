@@ -166,7 +166,8 @@ dmuon_status dmuon_plan_workspace_bytes(dmuon_plan_t plan, size_t* bytes);
  *  Builds the TMA tensor maps for the workspace buffers. The plan's host
  *  staging of the tables must outlive the copies: it does (it is owned by the
  *  plan). Returns DMUON_ERR_WORKSPACE if the buffer is NULL, misaligned or
- *  too small.
+ *  too small. A bind that fails after it has started writing the workspace
+ *  leaves the plan unbound (dmuon_step then returns DMUON_ERR_NOT_BOUND).
  */
 dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes, void* stream);
 

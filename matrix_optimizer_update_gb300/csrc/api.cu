@@ -821,6 +821,15 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   }
   P->ws = static_cast<char*>(d_workspace);
   char* ws = P->ws;
+  // From here on a failure leaves the plan unbound (a step then returns DMUON_ERR_NOT_BOUND)
+  // rather than bound to half-written tables.
+  struct Unbind {
+    dmuon_plan_s* plan;
+    bool done = false;
+    ~Unbind() {
+      if (!done) plan->ws = nullptr;
+    }
+  } unbind{P};
 
   // tables
   auto up = [&](int64_t off, const void* src, size_t n) -> cudaError_t {
@@ -954,20 +963,20 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   }
 
   // pinned staging for the per-step pointer tables
-  if (P->host_ptrs == nullptr) {
-    if ((e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
-      return cuda_fail(e, "cudaMallocHost");
-    if (P->off_wmaps >= 0 &&
-        (e = cudaMallocHost(&P->host_wmaps, sizeof(CUtensorMap) * P->mats.size() * kPtrSlots)) != cudaSuccess)
-      return cuda_fail(e, "cudaMallocHost");
-    for (int k = 0; k < kPtrSlots; ++k)
-      if ((e = cudaEventCreateWithFlags(&P->ptr_event[k], cudaEventDisableTiming)) != cudaSuccess)
-        return cuda_fail(e, "cudaEventCreate");
-  }
+  if (P->host_ptrs == nullptr && (e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
+    return cuda_fail(e, "cudaMallocHost");
+  if (P->off_wmaps >= 0 && P->host_wmaps == nullptr &&
+      (e = cudaMallocHost(&P->host_wmaps, sizeof(CUtensorMap) * P->mats.size() * kPtrSlots)) != cudaSuccess)
+    return cuda_fail(e, "cudaMallocHost");
+  for (int k = 0; k < kPtrSlots; ++k)
+    if (P->ptr_event[k] == nullptr &&
+        (e = cudaEventCreateWithFlags(&P->ptr_event[k], cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventCreate");
   for (int k = 0; k < kPtrSlots; ++k) {
     P->slot_ptrs[k].clear();
     P->slot_stamp[k] = 0;
   }
+  unbind.done = true;
   return DMUON_OK;
 }
 
