@@ -328,6 +328,115 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- our arm
+NS_KINDS = ("gram", "poly", "gemm", "symm")
+
+
+def alu_peak_tflops(peaks, local):
+    """fp32 FFMA peak: SMs x 128 lanes x 2 flops x max SM clock."""
+    import torch
+
+    props = torch.cuda.get_device_properties(local)
+    return props.multi_processor_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+
+
+def timed_steps(plan, step, steps, stream, launches_per_step, local, world, barrier, sample_clocks=True):
+    """Time ``steps`` calls of ``step`` with CUDA events on ``stream`` (after the caller's
+    warm-up), recording an event pair around every launch. Returns the elapsed ms (max over
+    ranks), the per-kind totals, the launches counted, the device status and the clocks."""
+    import torch
+
+    from matrix_optimizer_update_gb300 import dmuon as dm
+
+    clocks = ClockSampler(local) if sample_clocks else None
+    if clocks:
+        clocks.start()
+    plan.profile_begin(steps * launches_per_step)
+    c0 = plan.launch_count()
+    torch.cuda.synchronize()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = plan.launch_count() - c0
+    prof = plan.profile_end(steps * launches_per_step)
+    clk = clocks.stop() if clocks else None
+    status = plan.read_device_status(stream.cuda_stream)
+    per_kind = {}
+    for kind, kms, work in prof:
+        d = per_kind.setdefault(dm.KIND_NAMES[kind], {"ms": 0.0, "work": 0.0, "launches": 0})
+        d["ms"] += kms
+        d["work"] += work
+        d["launches"] += 1
+    return max_over_ranks(elapsed_ms, world, f"cuda:{local}"), per_kind, launches, status, clk
+
+
+def kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, compute, workload_name):
+    kernels = {}
+    for k, v in per_kind.items():
+        if k in NS_KINDS:
+            a = v["work"] / (v["ms"] * 1e-3) / 1e12
+            peak = alu_peak if compute == "f32" else tensor_peak
+            kernels[k] = {"ms_per_step": v["ms"] / steps, "tflops": a,
+                          ("frac_of_alu_peak" if compute == "f32" else "frac_of_tensor_peak"): a / peak}
+        else:
+            a = v["work"] / (v["ms"] * 1e-3) / 1e9
+            kernels[k] = {"ms_per_step": v["ms"] / steps, "gbs": a, "frac_of_hbm_peak": a / hbm_peak,
+                          "traffic": traffic_for(k, workload_name)}
+    return kernels
+
+
+def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
+    """Step time, Newton-Schulz throughput and per-kernel figures of one more matrix set (its own
+    inputs, plan and workspace, freed afterwards): the per_workload block of the bench line."""
+    import torch
+
+    from matrix_optimizer_update_gb300 import dmuon as dm
+    from matrix_optimizer_update_gb300 import workloads as wl
+    from matrix_optimizer_update_gb300.inputs import make_matrix_set
+
+    w = wl.get(name)
+    tot = wl.totals(w)
+    ms = make_matrix_set(w, f"cuda:{local}")
+    stream = torch.cuda.Stream()
+    muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
+                          grad=w.grad_dtype, compute=w.compute, device=f"cuda:{local}", stream=stream)
+    plan = muon.plan
+    lps = len(plan.describe()["launches"])
+    Wp, Gp, Mp = ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M)
+
+    def step():
+        plan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    steps = args.per_workload_steps
+    ms_tot, per_kind, launches, status, clk = timed_steps(plan, step, steps, stream, lps, local, 1, lambda: None)
+    ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in NS_KINDS) / steps
+    ns_tflops = tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None
+    peak = alu_peak if w.compute == "f32" else tensor_peak
+    out = {"matrices": tot["matrices"], "params": tot["params"], "ns_flops_per_step": tot["ns_flops"],
+           "steps": steps, "warmup": args.warmup, "ms_per_step": ms_tot / steps,
+           "value": aggregate(tot["ns_flops"], steps, 1, ms_tot * 1e-3),
+           "matrices_per_s": tot["matrices"] * steps / (ms_tot * 1e-3),
+           "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
+           ("ns_frac_of_alu_peak" if w.compute == "f32" else "ns_frac_of_sustained_peak"):
+               (ns_tflops / peak) if ns_tflops else None,
+           "compute": w.compute, "kernels": kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, w.compute,
+                                                         w.name),
+           "gpu_launches": launches, "device_status": status, "clocks": clk}
+    del muon, plan, ms
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -380,46 +489,19 @@ def run_ours(args):
     barrier()
 
     # ---- device-resident timed region
-    clocks = ClockSampler(local)
-    clocks.start()
-    plan.profile_begin(args.steps * launches_per_step)
-    c0 = plan.launch_count()
-    torch.cuda.synchronize()
-    barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    launches = plan.launch_count() - c0
-    prof = plan.profile_end(args.steps * launches_per_step)
-    clk = clocks.stop()
-    status = plan.read_device_status(sh)
-
-    max_ms = max_over_ranks(elapsed_ms, world, f"cuda:{local}")
+    max_ms, per_kind, launches, status, clk = timed_steps(plan, step, args.steps, stream, launches_per_step, local,
+                                                          world, barrier)
 
     # ---- per-kind accounting from the live events
-    per_kind = {}
-    for kind, kms, work in prof:
-        d = per_kind.setdefault(dm.KIND_NAMES[kind], {"ms": 0.0, "work": 0.0, "launches": 0})
-        d["ms"] += kms
-        d["work"] += work
-        d["launches"] += 1
-    NS_KINDS = ("gram", "poly", "gemm", "symm")
     ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in NS_KINDS) / args.steps
     peaks, peak_src = load_peaks()
     tensor_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alu_peak = alu_peak_tflops(peaks, local)
     ns_kinds = {k: v for k, v in per_kind.items() if k in NS_KINDS}
     dom = max(ns_kinds, key=lambda k: ns_kinds[k]["ms"]) if ns_kinds else max(per_kind, key=lambda k: per_kind[k]["ms"])
     d = per_kind[dom]
     if dom in NS_KINDS and w.compute == "f32":
-        # fp32 mode runs on the CUDA cores: FFMA peak = SMs x 128 lanes x 2 flops x max SM clock
-        props = torch.cuda.get_device_properties(local)
-        alu_peak = props.multi_processor_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
                 "frac": achieved / alu_peak, "peak_source": "SMs x 128 FP32 lanes x 2 x max SM clock",
@@ -437,54 +519,44 @@ def run_ours(args):
                 "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
                 "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
                 "traffic": traffic_for(dom, w.name)}
-    kernels = {}
-    for k, v in per_kind.items():
-        if k in NS_KINDS:
-            a = v["work"] / (v["ms"] * 1e-3) / 1e12
-            kernels[k] = {"ms_per_step": v["ms"] / args.steps, "tflops": a, "frac_of_tensor_peak": a / tensor_peak}
-        else:
-            a = v["work"] / (v["ms"] * 1e-3) / 1e9
-            kernels[k] = {"ms_per_step": v["ms"] / args.steps, "gbs": a, "frac_of_hbm_peak": a / hbm_peak,
-                          "traffic": traffic_for(k, w.name)}
+    kernels = kernel_table(per_kind, args.steps, tensor_peak, hbm_peak, alu_peak, w.compute, w.name)
 
-    # ---- the Gram-space form of the iteration on the same matrix set (reported beside the headline)
+    # ---- the Gram-space form of the iteration on the same matrix set (reported beside the headline):
+    # its speed-up over the standard form, and the throughput of the flops it actually executes
     gram = None
     if not args.no_gram and w.compute == "bf16":
         gm = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
                             grad=w.grad_dtype, compute=w.compute, flags=dm.FLAG_GRAM_NS | tile_flags,
-                            device=f"cuda:{local}",
-                            stream=stream)
+                            device=f"cuda:{local}", stream=stream)
         gplan = gm.plan
         glps = len(gplan.describe()["launches"])
+
+        def gstep():
+            gplan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
+
         for _ in range(args.warmup):
-            gplan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
+            gstep()
         torch.cuda.synchronize()
         barrier()
-        gplan.profile_begin(args.steps * glps)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
-            gplan.step(Wp, Gp, Mp, w.lr, w.mu, w.nesterov, sh)
-        g1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        gms = max_over_ranks(g0.elapsed_time(g1), world, f"cuda:{local}")
-        gprof = gplan.profile_end(args.steps * glps)
-        g_ns_ms = sum(kms for kind, kms, _ in gprof if dm.KIND_NAMES[kind] in NS_KINDS) / args.steps
-        g_ns_work = sum(wk for kind, _, wk in gprof if dm.KIND_NAMES[kind] in NS_KINDS) / args.steps
+        gms, gkind, _, gstatus, _ = timed_steps(gplan, gstep, args.steps, stream, glps, local, world, barrier,
+                                                sample_clocks=False)
+        g_ns_ms = sum(gkind.get(k, {}).get("ms", 0.0) for k in NS_KINDS) / args.steps
+        g_ns_work = sum(gkind.get(k, {}).get("work", 0.0) for k in NS_KINDS) / args.steps
         executed = g_ns_work / (g_ns_ms * 1e-3) / 1e12
         gram = {"ms_per_step": gms / args.steps, "ns_ms_per_step": g_ns_ms,
+                "speedup_vs_standard": (max_ms / args.steps) / (gms / args.steps),
                 "ns_flops_executed_per_step": g_ns_work,
-                "executed_tflops": executed, "executed_frac_of_peak": executed / tensor_peak,
-                "standard_equivalent_tflops": tot["ns_flops"] / (g_ns_ms * 1e-3) / 1e12,
-                "value": aggregate(tot["ns_flops"], args.steps, world, gms * 1e-3),
-                "launches_per_step": glps, "device_status": gplan.read_device_status(sh)}
+                "executed_tflops": executed, "executed_frac_of_sustained_peak": executed / tensor_peak,
+                "launches_per_step": glps, "device_status": gstatus}
         del gm, gplan
 
-    # ---- end to end through the public API: every step copies that step's gradients in from pinned
-    # host memory, runs dmuon_step and reads the step's result (its 4-byte status word) back to the
-    # host, which also synchronises. The copy of step k+1's gradients (into a second device buffer,
-    # on a copy stream) overlaps step k. A second figure also copies every updated weight back out.
+    # ---- end to end through the public API. Every step copies that step's gradients in from
+    # host memory, runs dmuon_step, and returns the step's results to the host: every updated
+    # weight, and the device status word (which also synchronises the host). The upload of step
+    # k+1's gradients (into a second device buffer, on a copy stream) overlaps step k; the copy of
+    # step k's weights (on a third stream) overlaps step k+1's momentum pass and its Newton-Schulz
+    # steps before the last: the library orders only its W-writing launches after that copy
+    # (dmuon_set_weight_events).
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(2, args.steps)  # as many steps as the device-timed region
@@ -494,11 +566,17 @@ def run_ours(args):
         hG.copy_(g_copy)
         ms.G.copy_(g_copy)
         del g_copy
+        hbW = fastest_host_buffer(ms.W, to_device=False)  # reads W, leaves it as it is
+        hW = hbW.tensor
         gbuf = [ms.G, torch.empty_like(ms.G)]
         gptrs = [Gp, ms.ptrs(gbuf[1])]
-        copy_stream = torch.cuda.Stream()
+        copy_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         used = [torch.cuda.Event(), torch.cuda.Event()]
+        w_ready, w_copied = torch.cuda.Event(), torch.cuda.Event()
+        w_ready.record(stream)  # creates both events (no work behind them yet)
+        w_copied.record(d2h_stream)
+        plan.set_weight_events(w_copied.cuda_event, w_ready.cuda_event)
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
@@ -516,40 +594,32 @@ def run_ours(args):
                     gbuf[nb].copy_(hG, non_blocking=True)
                     copied[nb].record(copy_stream)
             stream.wait_event(copied[b])
-            plan.step(Wp, gptrs[b], Mp, w.lr, w.mu, w.nesterov, sh)
+            plan.step(Wp, gptrs[b], Mp, w.lr, w.mu, w.nesterov, sh)  # W writes wait for w_copied
             used[b].record(stream)
+            with torch.cuda.stream(d2h_stream):  # this step's weights back to the host
+                d2h_stream.wait_event(w_ready)
+                hW.copy_(ms.W, non_blocking=True)
+                w_copied.record(d2h_stream)
             bits |= plan.read_device_status(sh)
         torch.cuda.synchronize()
         wall_ms = (time.perf_counter() - t0) * 1e3
+        plan.set_weight_events(0, 0)
+        returned_ok = bool(torch.equal(hW.to(ms.W.device), ms.W))
         barrier()
         e2e_ms = max_over_ranks(wall_ms, world, f"cuda:{local}")
         e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
-               "h2d_bytes_per_step": hG.numel() * hG.element_size(), "d2h_bytes_per_step": 4,
-               "result_read": "device status word (dmuon_read_device_status), every step",
-               "timing": "host wall clock from the first upload to the last status read",
-               "overlap": "next step's gradient upload overlaps the current step (two device buffers)",
-               "host_memory": f"{hbG.kind} (the faster of two kinds on this machine: {hbG.rate_gbs:.0f} GB/s to the device)",
+               "h2d_bytes_per_step": hG.numel() * hG.element_size(),
+               "d2h_bytes_per_step": hW.numel() * hW.element_size() + 4,
+               "result_read": "every updated weight (to host memory) and the device status word, every step",
+               "returned_weights_match_device": returned_ok,
+               "timing": "host wall clock from the first upload to the end of the last weight copy",
+               "overlap": "next step's gradient upload overlaps the current step (two device buffers); each step's "
+                          "weight copy overlaps the next step up to its last Newton-Schulz product",
+               "host_memory": f"grads: {hbG.kind} ({hbG.rate_gbs:.0f} GB/s to the device); weights: {hbW.kind} "
+                              f"({hbW.rate_gbs:.0f} GB/s from the device); the faster of two kinds each",
                "device_status": bits}
         del gbuf[1]
-        hbW = fastest_host_buffer(ms.W, to_device=False)  # reads W, leaves it as it is
-        hW = hbW.tensor
-        torch.cuda.synchronize()
-        barrier()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(e2e_steps):
-                ms.G.copy_(hG, non_blocking=True)
-                step()
-                hW.copy_(ms.W, non_blocking=True)
-        f1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        full_ms = max_over_ranks(f0.elapsed_time(f1), world, f"cuda:{local}")
-        e2e["with_weight_readback"] = {"value": aggregate(tot["ns_flops"], e2e_steps, world, full_ms * 1e-3),
-                                       "ms_per_step": full_ms / e2e_steps,
-                                       "d2h_bytes_per_step": hW.numel() * hW.element_size()}
         del hG, hW
         torch.cuda.synchronize()
         hbG.release()
@@ -585,6 +655,17 @@ def run_ours(args):
                  "bytes_per_element": 22, "launches_per_step": 1}
         del ap, ag, am, av
 
+    # ---- the other matrix sets, one at a time (one GPU only; each with its own inputs and plan)
+    del muon, plan, ms
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    per_workload = None
+    if world == 1 and not args.no_per_workload and not (args.layers or args.experts):
+        per_workload = {}
+        for name in wl.WORKLOADS:
+            if name != w.name:
+                per_workload[name] = measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s, f, names = oracle_sample(w, args.cpu_budget)
@@ -595,6 +676,7 @@ def run_ours(args):
                "extrapolated_step_ms": tot["ns_flops"] / (f / s) * 1e3}
 
     value = aggregate(tot["ns_flops"], args.steps, world, max_ms * 1e-3)
+    ns_tflops = tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -605,9 +687,10 @@ def run_ours(args):
                    "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
-        "ns_ms_per_step": ns_ms, "ns_tflops": tot["ns_flops"] / (ns_ms * 1e-3) / 1e12 if ns_ms else None,
-        "ns_frac_of_peak": (tot["ns_flops"] / (ns_ms * 1e-3) / 1e12) / tensor_peak if ns_ms else None,
+        "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
+        "ns_frac_of_sustained_peak": ns_tflops / tensor_peak if ns_tflops else None,
         "kernels": kernels, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
+        "per_workload": per_workload,
         **({"adamw_other_params": adamw} if adamw is not None else {}),
         "gpu_launches": launches,
         "clocks": clk, "device_status": status,
@@ -634,6 +717,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the other matrix sets")
+    ap.add_argument("--per-workload-steps", type=int, default=5, help="timed steps per other matrix set")
     ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
     ap.add_argument("--adamw", action="store_true",
                     help="also time the AdamW kernel over Llama-3.1-8B's non-matrix parameters")

@@ -165,9 +165,14 @@ dmuon_status dmuon_plan_workspace_bytes(dmuon_plan_t plan, size_t* bytes);
  *               again. Its contents need not be initialised.
  *  Builds the TMA tensor maps for the workspace buffers. The plan's host
  *  staging of the tables must outlive the copies: it does (it is owned by the
- *  plan). Returns DMUON_ERR_WORKSPACE if the buffer is NULL, misaligned or
- *  too small. A bind that fails after it has started writing the workspace
- *  leaves the plan unbound (dmuon_step then returns DMUON_ERR_NOT_BOUND).
+ *  plan). Returns DMUON_ERR_WORKSPACE if the buffer is NULL, misaligned, too
+ *  small or not memory of the current device, DMUON_ERR_UNSUPPORTED for bf16 compute on a GPU other than
+ *  sm_103. Any failing bind leaves the plan unbound, also a plan that was
+ *  bound before (dmuon_step then returns DMUON_ERR_NOT_BOUND until a bind
+ *  succeeds). For tests, the environment variable DMUON_TEST_FAIL set to
+ *  bind_check, bind_tables, bind_maps or bind_staging makes the bind fail at
+ *  that point (before any CUDA call, after the tables are uploaded, while the
+ *  tensor maps are built, or before the host staging is allocated).
  */
 dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes, void* stream);
 
@@ -203,6 +208,30 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t plan, void* d_workspace, size_t bytes,
  */
 dmuon_status dmuon_step(dmuon_plan_t plan, void* const* params, const void* const* grads,
                         void* const* momenta, float lr, float mu, int32_t nesterov, void* stream);
+
+/*
+ * dmuon_set_weight_events - order the weight writes of later steps against
+ * work on other streams. Only the launches that write W (the last
+ * Newton-Schulz product of each launch chunk, or the update kernel when
+ * ns_steps == 0) touch the weights; the momentum pass and every earlier
+ * product read only the gradients, the momenta and the workspace.
+ *
+ *  wait_before_write  a cudaEvent_t (as void*) or NULL: every later
+ *                     dmuon_step makes its stream wait on it
+ *                     (cudaStreamWaitEvent, on the event's most recent
+ *                     record at the time of that dmuon_step call) just
+ *                     before its first launch that writes W.
+ *  after_write        a cudaEvent_t or NULL: every later dmuon_step
+ *                     records it on its stream right after its last launch
+ *                     that writes W.
+ *
+ * With both, a copy of step k's weights (to the host, say) can run on
+ * another stream while step k+1's momentum pass and its first ns_steps - 1
+ * Newton-Schulz steps run: the copy waits on after_write and records
+ * wait_before_write. The events stay the caller's; they must stay valid
+ * while set (NULL, NULL clears them). Host only; no effect on the results.
+ */
+dmuon_status dmuon_set_weight_events(dmuon_plan_t plan, void* wait_before_write, void* after_write);
 
 /*
  * dmuon_read_device_status - synchronise stream, return the device status
@@ -286,8 +315,11 @@ dmuon_status dmuon_selftest_wait_timeout(void* d_scratch, int64_t limit_ns, void
  * larger matrices return DMUON_ERR_UNSUPPORTED. The static array (256 KiB +
  * 256 B) stays allocated on every GPU that loads the library until the
  * process exits. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. The call allocates nothing: it launches two
+ * address (cudaGetSymbolAddress) with that device current, and so does the
+ * first call after the device's context was replaced (cudaDeviceReset); make
+ * that first call before any stream capture. A CUDA error that earlier work
+ * left pending is reported (DMUON_ERR_CUDA, left pending) before anything is
+ * launched. The call allocates nothing: it launches two
  * kernels on stream (the tile pass, which writes one partial sum per tile,
  * and a one-block kernel that adds them in a fixed order and writes s_out).
  * 16-byte aligned grad, momentum and u_out (with cols % 4 == 0) take the

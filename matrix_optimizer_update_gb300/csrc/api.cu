@@ -14,11 +14,13 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <tuple>
@@ -34,6 +36,26 @@ namespace {
 
 thread_local std::string g_err;
 
+// DMUON_LOG=1 in the environment: the library writes one line per plan, bind,
+// first step of a plan and error to stderr. Otherwise it writes nothing.
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("DMUON_LOG");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+void logf(const char* fmt, ...) {
+  if (!log_enabled()) return;
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  std::fprintf(stderr, "[dmuon] %s\n", buf);
+}
+
 dmuon_status fail(dmuon_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -41,7 +63,23 @@ dmuon_status fail(dmuon_status st, const char* fmt, ...) {
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
   g_err = buf;
+  logf("error %d: %s", static_cast<int>(st), buf);
   return st;
+}
+
+// NVTX range names per launch kind (host-side ranges around each launch of a
+// step; free when no profiling tool is attached).
+const char* kind_range_name(int kind) {
+  switch (kind) {
+    case DMUON_KIND_MOMENTUM: return "dmuon momentum";
+    case DMUON_KIND_GRAM: return "dmuon gram X X^T";
+    case DMUON_KIND_POLY: return "dmuon poly aI + bA + cA^2";
+    case DMUON_KIND_GEMM: return "dmuon gemm P X";
+    case DMUON_KIND_UPDATE0: return "dmuon update (ns_steps 0)";
+    case DMUON_KIND_SYMM: return "dmuon symm (Gram form)";
+    case DMUON_KIND_NORM: return "dmuon norm";
+    default: return "dmuon launch";
+  }
 }
 
 dmuon_status cuda_fail(cudaError_t e, const char* what) {
@@ -54,6 +92,14 @@ int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int kPtrSlots = 4;  // device-resident pointer tables per plan
+
+// Host-side failure injection for tests: true when the environment variable
+// DMUON_TEST_FAIL names this point of dmuon_plan_bind. Nothing on the device
+// is involved; the call then fails as if the CUDA call at that point had.
+bool test_hook(const char* where) {
+  const char* v = std::getenv("DMUON_TEST_FAIL");
+  return v != nullptr && std::strcmp(v, where) == 0;
+}
 
 // Workspace buffers of a bucket, by role. Standard buckets use X0/X1 (the
 // iterate, ping-pong), A and B; Gram-space buckets use X0 (U, read twice), G,
@@ -166,7 +212,12 @@ struct dmuon_plan_s {
   std::vector<int32_t> prof_kind;
   std::vector<double> prof_work;
   int64_t launch_count = 0;
+  int64_t steps_taken = 0;
   bool tuned = false;
+  // ---- ordering of the weight writes against other streams (dmuon_set_weight_events)
+  cudaEvent_t w_wait = nullptr;   // waited on before the first launch that writes W
+  cudaEvent_t w_done = nullptr;   // recorded after the last launch that writes W
+  int first_w_launch = -1, last_w_launch = -1;  // indices into launches
 };
 
 namespace {
@@ -510,6 +561,15 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
     }
     add(DMUON_KIND_GEMM, kPhaseGemm, S - 1, c, kListGemm, qbuf(S + 1), kBufX0, kBufNone, kBufX0, 0.f, 0, 0, 0, 1, 1);
   }
+  // the launches that write W: the update kernel (ns_steps = 0) or the last product of each chunk
+  P.first_w_launch = P.last_w_launch = -1;
+  for (size_t l = 0; l < P.launches.size(); ++l) {
+    const Launch& x = P.launches[l];
+    if (x.kind == DMUON_KIND_UPDATE0 || (x.kind == DMUON_KIND_GEMM && x.last)) {
+      if (P.first_w_launch < 0) P.first_w_launch = static_cast<int>(l);
+      P.last_w_launch = static_cast<int>(l);
+    }
+  }
   return DMUON_OK;
 }
 
@@ -784,6 +844,13 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
     delete P;
     return st;
   }
+  logf("plan %p: %d matrices, %zu buckets, %zu launch chunks, %zu launches per step, ns_steps %d, compute %s, "
+       "flags 0x%x, workspace %zu bytes",
+       (void*)P, n_mats, P->buckets.size(), P->chunks.size(), P->launches.size(), ns_steps, P->tc ? "bf16" : "f32",
+       flags, P->ws_bytes);
+  for (const BucketPlan& B : P->buckets)
+    logf("  bucket %d x %d: %d matrices (%d transposed), form %s, tile widths %d/%d%s", B.m, B.n, B.count,
+         B.n_transposed, B.gram ? "gram" : "standard", B.bn_sym, B.bn_gemm, B.pair ? ", pairs" : "");
   *out = P;
   return DMUON_OK;
 }
@@ -797,39 +864,48 @@ dmuon_status dmuon_plan_workspace_bytes(dmuon_plan_t P, size_t* bytes) {
 dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, void* stream) {
   g_err.clear();
   if (P == nullptr) return fail(DMUON_ERR_INVALID_ARG, "plan is NULL");
+  // Every failing return below leaves the plan unbound (a step then returns DMUON_ERR_NOT_BOUND),
+  // whether it was bound before or not: never bound to half-written tables, nor to a workspace
+  // of one device with the device and SM count of another.
+  struct Unbind {
+    dmuon_plan_s* plan;
+    bool done = false;
+    ~Unbind() {
+      if (!done) {
+        plan->ws = nullptr;
+        plan->device = -1;
+      }
+    }
+  } unbind{P};
   if (d_workspace == nullptr) return fail(DMUON_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(d_workspace) % kAlign != 0)
     return fail(DMUON_ERR_WORKSPACE, "workspace must be %lld-byte aligned", (long long)kAlign);
   if (bytes < P->ws_bytes)
     return fail(DMUON_ERR_WORKSPACE, "workspace has %zu bytes, plan needs %zu", bytes, P->ws_bytes);
+  if (test_hook("bind_check")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_check)");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if ((e = cudaGetDevice(&P->device)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if ((e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device)) != cudaSuccess)
+  int device = -1, num_sms = 0;
+  if ((e = cudaGetDevice(&device)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if ((e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute");
   cudaPointerAttributes pa;
-  if (cudaPointerGetAttributes(&pa, d_workspace) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+  if (cudaPointerGetAttributes(&pa, d_workspace) != cudaSuccess || pa.type != cudaMemoryTypeDevice ||
+      pa.device != device) {
     cudaGetLastError();
-    return fail(DMUON_ERR_WORKSPACE, "workspace is not device memory");
+    return fail(DMUON_ERR_WORKSPACE, "workspace is not device memory of the current device %d", device);
   }
   if (P->tc) {
     int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, P->device);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, P->device);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
     if (major != 10 || minor != 3)
       return fail(DMUON_ERR_UNSUPPORTED, "bf16 compute needs an sm_103 GPU (found sm_%d%d)", major, minor);
   }
   P->ws = static_cast<char*>(d_workspace);
+  P->device = device;
+  P->num_sms = num_sms;
   char* ws = P->ws;
-  // From here on a failure leaves the plan unbound (a step then returns DMUON_ERR_NOT_BOUND)
-  // rather than bound to half-written tables.
-  struct Unbind {
-    dmuon_plan_s* plan;
-    bool done = false;
-    ~Unbind() {
-      if (!done) plan->ws = nullptr;
-    }
-  } unbind{P};
 
   // tables
   auto up = [&](int64_t off, const void* src, size_t n) -> cudaError_t {
@@ -845,6 +921,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   if ((e = cudaMemsetAsync(ws + P->off_status, 0, P->off_s - P->off_status, s)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "bind sync");
+  if (test_hook("bind_tables")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_tables)");
 
   // momentum-pass parameters
   StreamParams& sp = P->sp;
@@ -898,6 +975,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       for (size_t lb = 0; lb < ch.size(); ++lb) {
         const BucketPlan& B = P->buckets[ch[lb]];
         // a pair's CTAs each load 128 rows of a K-major B operand
+        if (test_hook("bind_maps")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_maps)");
         dmuon_status st = fill_tc_bucket(*P, B, L.phase, L.pair ? 128 : L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb]);
         if (st != DMUON_OK) return st;
       }
@@ -963,6 +1041,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   }
 
   // pinned staging for the per-step pointer tables
+  if (test_hook("bind_staging")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_staging)");
   if (P->host_ptrs == nullptr && (e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
     return cuda_fail(e, "cudaMallocHost");
   if (P->off_wmaps >= 0 && P->host_wmaps == nullptr &&
@@ -977,6 +1056,8 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
     P->slot_stamp[k] = 0;
   }
   unbind.done = true;
+  logf("bind %p: device %d, %d SMs, workspace %p (%zu bytes)%s", (void*)P, P->device, P->num_sms, (void*)P->ws,
+       bytes, P->tuned ? ", tuned" : "");
   return DMUON_OK;
 }
 
@@ -1052,7 +1133,22 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
   sp.lr = lr;
   sp.nesterov = nesterov;
   sp.ptrs = dptrs;
-  for (const Launch& L : P->launches) {
+  if (P->steps_taken++ == 0)
+    logf("step: plan %p, first step: %zu launches, pointer slot %d, lr %g mu %g nesterov %d", (void*)P,
+         P->launches.size(), slot, lr, mu, nesterov);
+  struct NvtxStep {
+    NvtxStep() { nvtxRangePushA("dmuon_step"); }
+    ~NvtxStep() { nvtxRangePop(); }
+  } nvtx_step;
+  for (size_t li = 0; li < P->launches.size(); ++li) {
+    const Launch& L = P->launches[li];
+    struct NvtxLaunch {
+      explicit NvtxLaunch(int kind) { nvtxRangePushA(kind_range_name(kind)); }
+      ~NvtxLaunch() { nvtxRangePop(); }
+    } nvtx_launch(L.kind);
+    if (static_cast<int>(li) == P->first_w_launch && P->w_wait != nullptr &&
+        (e = cudaStreamWaitEvent(s, P->w_wait, 0)) != cudaSuccess)
+      return cuda_fail(e, "cudaStreamWaitEvent (weight events)");
     dmuon_status st = record_launch(*P, L, s, true);
     if (st != DMUON_OK) return st;
     if (L.kind == DMUON_KIND_MOMENTUM) {
@@ -1077,7 +1173,18 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     ++P->launch_count;
     st = record_launch(*P, L, s, false);
     if (st != DMUON_OK) return st;
+    if (static_cast<int>(li) == P->last_w_launch && P->w_done != nullptr &&
+        (e = cudaEventRecord(P->w_done, s)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventRecord (weight events)");
   }
+  return DMUON_OK;
+}
+
+dmuon_status dmuon_set_weight_events(dmuon_plan_t P, void* wait_before_write, void* after_write) {
+  g_err.clear();
+  if (P == nullptr) return fail(DMUON_ERR_INVALID_ARG, "plan is NULL");
+  P->w_wait = reinterpret_cast<cudaEvent_t>(wait_before_write);
+  P->w_done = reinterpret_cast<cudaEvent_t>(after_write);
   return DMUON_OK;
 }
 

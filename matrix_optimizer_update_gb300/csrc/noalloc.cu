@@ -18,9 +18,12 @@
 // 64 x 128 tile code as the workspace pass, stream_tile.cuh), where every
 // tile writes its partial sum of squares, then one CTA that adds the
 // partials in a fixed order in fp64 and writes s.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cmath>
 #include <mutex>
 
@@ -96,10 +99,41 @@ __global__ void __launch_bounds__(kStreamThreads) noalloc_finalize_kernel(const 
   }
 }
 
-// Device address of the static scratch, looked up once per device.
+// Device address of the static scratch, looked up once per device and
+// context. The address belongs to the context that was current when it was
+// looked up: after cudaDeviceReset the device gets a new primary context,
+// whose ID differs, and the address is looked up again.
 constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // unique over the process's lifetime; 0 = not looked up
+  unsigned* addr = nullptr;
+};
 std::mutex g_setup_mu;
-unsigned* g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+// ID of the calling thread's current context, or 0 when none is current yet.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    looked_up = true;
+  }
+  if (get_cur == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 }  // namespace
 }  // namespace dmuon
@@ -127,18 +161,31 @@ extern "C" dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* mom
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return set_last_error(DMUON_ERR_CUDA, "no usable current CUDA device");
+  // An error left pending by the caller's earlier work is reported as such (and left pending),
+  // not mistaken for a failure of this call's launches.
+  const cudaError_t pending = cudaPeekAtLastError();
+  if (pending != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "a CUDA error from earlier work is pending: %s (%s)", cudaGetErrorName(pending),
+             cudaGetErrorString(pending));
+    return set_last_error(DMUON_ERR_CUDA, msg);
+  }
   unsigned* scratch;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchAddr& sa = g_scratch_addr[dev];
+    unsigned long long ctx = current_context_id();
+    if (sa.addr == nullptr || ctx == 0 || ctx != sa.ctx_id) {
       // The array's name in host code is only a host-side handle; the kernel
-      // needs its device address, fetched here with this device current.
+      // needs its device address, fetched here with this device current (this
+      // also creates the device's primary context when none exists yet).
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
         return set_last_error(DMUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-      g_scratch_addr[dev] = static_cast<unsigned*>(ptr);
+      sa.addr = static_cast<unsigned*>(ptr);
+      sa.ctx_id = current_context_id();
     }
-    scratch = g_scratch_addr[dev];
+    scratch = sa.addr;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -173,8 +220,9 @@ extern "C" dmuon_status dmuon_momentum_norm_noalloc(const void* grad, float* mom
     momentum_noalloc_kernel<false, true><<<grid, kStreamThreads, 0, s>>>(p);
   else
     momentum_noalloc_kernel<false, false><<<grid, kStreamThreads, 0, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "kernel launch failed");
+  // no error was pending before the launches, so one seen now is theirs
+  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "tile-pass kernel launch failed");
   noalloc_finalize_kernel<<<1, kStreamThreads, 0, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "kernel launch failed");
+  if (cudaGetLastError() != cudaSuccess) return set_last_error(DMUON_ERR_CUDA, "norm kernel launch failed");
   return set_last_error(DMUON_OK, "");
 }

@@ -44,7 +44,7 @@ KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0", 5: "
 # every symbol include/dmuon.h declares
 EXPORTS = (
     "dmuon_plan", "dmuon_plan_workspace_bytes", "dmuon_plan_bind", "dmuon_step",
-    "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
+    "dmuon_set_weight_events", "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
     "dmuon_profile_begin", "dmuon_profile_end", "dmuon_plan_costs", "dmuon_launch_count",
     "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_assign_owners", "dmuon_adamw_flat",
     "dmuon_plan_destroy", "dmuon_last_error", "dmuon_version",
@@ -85,6 +85,7 @@ def lib():
         "dmuon_plan_workspace_bytes": (i32, [vp, ctypes.POINTER(sz)]),
         "dmuon_plan_bind": (i32, [vp, vp, sz, vp]),
         "dmuon_step": (i32, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), f32, f32, i32, vp]),
+        "dmuon_set_weight_events": (i32, [vp, vp, vp]),
         "dmuon_read_device_status": (i32, [vp, vp, ctypes.POINTER(u32)]),
         "dmuon_read_update": (i32, [vp, i32, vp, vp]),
         "dmuon_plan_describe": (i32, [vp, ctypes.c_char_p, sz, ctypes.POINTER(sz)]),
@@ -176,6 +177,11 @@ class Plan:
         _, pa, ga, ma = self._ptr_cache
         _check(lib().dmuon_step(self._h, pa, ga, ma, float(lr), float(mu), int(bool(nesterov)),
                                 ctypes.c_void_p(stream)))
+
+    def set_weight_events(self, wait_before_write: int = 0, after_write: int = 0):
+        """cudaEvent_t handles (ints, 0 = none): see dmuon_set_weight_events."""
+        _check(lib().dmuon_set_weight_events(self._h, ctypes.c_void_p(wait_before_write or None),
+                                             ctypes.c_void_p(after_write or None)))
 
     def read_device_status(self, stream: int = 0) -> int:
         b = ctypes.c_uint32()

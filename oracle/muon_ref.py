@@ -36,7 +36,7 @@ and the closed form of the momentum recurrence.
 from __future__ import annotations
 
 import math
-from typing import Iterable, Sequence
+from typing import Sequence
 
 import numpy as np
 
@@ -199,7 +199,3 @@ def round_to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
         return np.asarray(x, dtype=np.float64)
     raise ValueError(f"unknown dtype {dtype!r}")
 
-
-def muon_step_batch(Ws: Iterable, Gs: Iterable, Ms: Iterable, **kw):
-    """Apply :func:`muon_step` independently to every matrix of a batch."""
-    return [muon_step(W, G, M, **kw) for W, G, M in zip(Ws, Gs, Ms)]

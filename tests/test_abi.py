@@ -4,6 +4,8 @@ counts tiles as stated."""
 
 import os
 import re
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -70,6 +72,33 @@ def test_step_before_bind_is_refused():
     with pytest.raises(dm.DmuonError) as e:
         p.read_update(0, 1024, 0)
     assert e.value.status == dm.ERR_UNSUPPORTED
+
+
+def test_failed_bind_leaves_the_plan_unbound(monkeypatch):
+    # the host-side failure hook fires before any CUDA call: no GPU needed
+    p = dm.dmuon_plan([(8, 16)], 5)
+    monkeypatch.setenv("DMUON_TEST_FAIL", "bind_check")
+    with pytest.raises(dm.DmuonError) as e:
+        p.bind(1 << 30, p.workspace_bytes(), 0)
+    assert e.value.status == dm.ERR_CUDA and "injected failure" in str(e.value)
+    monkeypatch.delenv("DMUON_TEST_FAIL")
+    with pytest.raises(dm.DmuonError) as e:
+        p.step([16], [32], [48], 0.02, 0.95, True, 0)
+    assert e.value.status == dm.ERR_NOT_BOUND
+
+
+def test_log_switch_writes_plan_lines_to_stderr():
+    code = ("from matrix_optimizer_update_gb300 import dmuon as dm; "
+            "p = dm.dmuon_plan([(256, 384), (384, 256), (64, 64)], 5); p.destroy()")
+    env = dict(os.environ, DMUON_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stderr.splitlines() if x.startswith("[dmuon]")]
+    assert any("plan" in x and "3 matrices" in x for x in lines), r.stderr
+    assert sum(x.startswith("[dmuon]   bucket") for x in lines) == 2, r.stderr
+    env.pop("DMUON_LOG")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT, timeout=120)
+    assert r.returncode == 0 and "[dmuon]" not in r.stderr
 
 
 def cdiv(a, b):
