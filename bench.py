@@ -375,6 +375,38 @@ def timed_steps(plan, step, steps, stream, launches_per_step, local, world, barr
     return max_over_ranks(elapsed_ms, world, f"cuda:{local}"), per_kind, launches, status, clk
 
 
+def cta_tails(plan, step, stream):
+    """One more step with per-CTA start/end records; per kind of tensor-core launch, the tail
+    (last CTA's end minus the median CTA's end) as a fraction of the launch's span (first start to
+    last end), worst and mean over the step's launches, and the fraction of CTA time left idle."""
+    import statistics as st
+
+    import torch
+
+    from matrix_optimizer_update_gb300 import dmuon as dm
+
+    plan.profile_cta_times(True)
+    step()
+    torch.cuda.synchronize()
+    out = {}
+    for li, L in enumerate(plan.describe()["launches"]):
+        rec = plan.read_cta_times(li, stream.cuda_stream)
+        if not rec:
+            continue
+        t0 = min(a for a, _ in rec)
+        ends = sorted(b for _, b in rec)
+        span = ends[-1] - t0
+        if span <= 0:
+            continue
+        busy = sum(b - a for a, b in rec)
+        d = out.setdefault(dm.KIND_NAMES[L["kind"]], {"tails": [], "idle": []})
+        d["tails"].append((ends[-1] - st.median(ends)) / span)
+        d["idle"].append(1.0 - busy / (len(rec) * span))
+    plan.profile_cta_times(False)
+    return {k: {"tail_frac_max": max(v["tails"]), "tail_frac_mean": st.fmean(v["tails"]),
+                "idle_frac_mean": st.fmean(v["idle"]), "launches": len(v["tails"])} for k, v in out.items()}
+
+
 def kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, compute, workload_name):
     kernels = {}
     for k, v in per_kind.items():
@@ -404,7 +436,8 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
     ms = make_matrix_set(w, f"cuda:{local}")
     stream = torch.cuda.Stream()
     muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
-                          grad=w.grad_dtype, compute=w.compute, device=f"cuda:{local}", stream=stream)
+                          grad=w.grad_dtype, compute=w.compute, flags=plan_flags(args), device=f"cuda:{local}",
+                          stream=stream)
     plan = muon.plan
     lps = len(plan.describe()["launches"])
     Wp, Gp, Mp = ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M)
@@ -430,11 +463,18 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
                (ns_tflops / peak) if ns_tflops else None,
            "compute": w.compute, "kernels": kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, w.compute,
                                                          w.name),
-           "gpu_launches": launches, "device_status": status, "clocks": clk}
+           "gpu_launches": launches, "device_status": status, "clocks": clk,
+           "cta_tails": cta_tails(plan, step, stream) if w.compute == "bf16" else None}
     del muon, plan, ms
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
+
+
+def plan_flags(args):
+    from matrix_optimizer_update_gb300 import dmuon as dm
+
+    return (dm.FLAG_PAIR_TILES if args.pair else 0) | (dm.FLAG_STATIC_TILES if args.static_tiles else 0)
 
 
 def run_ours(args):
@@ -463,7 +503,7 @@ def run_ours(args):
     tot = wl.totals(w)
     ms = make_matrix_set(w, f"cuda:{local}", seed_offset=replica_seed_offset(rank))
     stream = torch.cuda.Stream()
-    tile_flags = dm.FLAG_PAIR_TILES if args.pair else 0
+    tile_flags = plan_flags(args)
     muon = dm.Muon.create(w.shapes, ns_steps=w.ns_steps, coeffs=w.coeffs, eps=w.eps, param=w.param_dtype,
                           grad=w.grad_dtype, compute=w.compute, flags=tile_flags, device=f"cuda:{local}",
                           stream=stream)
@@ -520,6 +560,7 @@ def run_ours(args):
                 "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
                 "traffic": traffic_for(dom, w.name)}
     kernels = kernel_table(per_kind, args.steps, tensor_peak, hbm_peak, alu_peak, w.compute, w.name)
+    tails = cta_tails(plan, step, stream) if w.compute == "bf16" else None
 
     # ---- the Gram-space form of the iteration on the same matrix set (reported beside the headline):
     # its speed-up over the standard form, and the throughput of the flops it actually executes
@@ -685,11 +726,12 @@ def run_ours(args):
                    "ns_steps": w.ns_steps, "ns_flops_per_step": tot["ns_flops"],
                    "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
                    "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
+                   "tile_schedule": "dealt round-robin" if args.static_tiles else "claimed from a counter",
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
         "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
         "ns_frac_of_sustained_peak": ns_tflops / tensor_peak if ns_tflops else None,
-        "kernels": kernels, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
+        "kernels": kernels, "cta_tails": tails, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
         "per_workload": per_workload,
         **({"adamw_other_params": adamw} if adamw is not None else {}),
         "gpu_launches": launches,
@@ -720,6 +762,7 @@ def main(argv=None):
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other matrix sets")
     ap.add_argument("--per-workload-steps", type=int, default=5, help="timed steps per other matrix set")
     ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
+    ap.add_argument("--static-tiles", action="store_true", help="deal tiles round-robin instead of claiming them")
     ap.add_argument("--adamw", action="store_true",
                     help="also time the AdamW kernel over Llama-3.1-8B's non-matrix parameters")
     args = ap.parse_args(argv)

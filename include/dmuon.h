@@ -107,6 +107,12 @@ typedef struct {
                                           no X_k tile: the same polynomial, one
                                           bf16 rounding of a + B_ii instead of
                                           an fp32 a*X term.                      */
+#define DMUON_FLAG_STATIC_TILES 0x20u  /* one-SM tensor-core launches deal the cost-ordered
+                                          tile list round-robin (CTA b takes tiles b,
+                                          b + grid, ...) instead of letting each CTA
+                                          claim the next tile from the launch's counter
+                                          as it becomes free. Same results bit for bit;
+                                          kept to compare the two schedules.       */
 #define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
                                           per bucket on the bound workspace, keep
                                           the faster, and order tiles by measured
@@ -280,6 +286,22 @@ dmuon_status dmuon_profile_end(dmuon_plan_t plan, int32_t* kinds, float* ms, dou
  * balanced on measured, not theoretical, costs).
  */
 dmuon_status dmuon_plan_costs(dmuon_plan_t plan, double* per_matrix_ms, int32_t n);
+
+/*
+ * Per-CTA timing of the tensor-core launches (profiling). After
+ * dmuon_profile_cta_times(plan, 1), every tensor-core launch of the following
+ * steps records, per CTA, the global timer (ns) when the CTA started and when
+ * it finished, in the workspace (each step overwrites the previous one's);
+ * dmuon_profile_cta_times(plan, 0) stops it. dmuon_read_cta_times copies the
+ * records of launch `launch` (its index in dmuon_plan_describe's launch list)
+ * of the last recorded step to out[2*i] (start) and out[2*i+1] (end) for CTA
+ * i < min(cap, *n_ctas), host memory, synchronising stream; *n_ctas receives
+ * the launch's CTA count (0 for launches that keep no records: streaming
+ * kernels, fp32 mode and CTA pairs).
+ */
+dmuon_status dmuon_profile_cta_times(dmuon_plan_t plan, int32_t enable);
+dmuon_status dmuon_read_cta_times(dmuon_plan_t plan, int32_t launch, uint64_t* out, int32_t cap, int32_t* n_ctas,
+                                  void* stream);
 
 /* Number of kernels the library has launched through this plan so far. */
 dmuon_status dmuon_launch_count(dmuon_plan_t plan, int64_t* count);

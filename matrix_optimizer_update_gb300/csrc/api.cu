@@ -88,6 +88,7 @@ dmuon_status cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int64_t kAlign = 1024;
 constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
+constexpr int64_t kSchedBytes = 128;   // one launch's tile-claim counters (own cache line)
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -183,7 +184,8 @@ struct dmuon_plan_s {
   // ---- workspace layout (byte offsets)
   size_t ws_bytes = 0;
   int64_t off_status = 0, off_s = 0, off_partial = 0, off_mats = 0, off_ub = 0, off_ptrs = 0,
-          off_items = 0, off_probe = 0, off_capture = -1, off_wmaps = -1;
+          off_items = 0, off_probe = 0, off_capture = -1, off_wmaps = -1, off_sched = 0, off_cta = 0,
+          off_probe_sched = 0;
   int64_t cap_elems = 0;
   // ---- binding
   char* ws = nullptr;
@@ -214,6 +216,7 @@ struct dmuon_plan_s {
   int64_t launch_count = 0;
   int64_t steps_taken = 0;
   bool tuned = false;
+  bool cta_times = false;  // dmuon_profile_cta_times: record per-CTA start/end of tensor-core launches
   // ---- ordering of the weight writes against other streams (dmuon_set_weight_events)
   cudaEvent_t w_wait = nullptr;   // waited on before the first launch that writes W
   cudaEvent_t w_done = nullptr;   // recorded after the last launch that writes W
@@ -245,15 +248,18 @@ int dtype_bytes(int32_t d) { return d == DMUON_BF16 ? 2 : 4; }
 // is the default unless its tiles, weighted by 1.4, outnumber those of 128.
 constexpr double kWideTileCost = 1.4;
 
-int64_t sym_tiles(int m, int bn) {  // tiles touching the upper triangle of m x m (128-row blocks)
-  const int64_t tn = cdiv(m, bn);
+// Tiles of a symmetric m x m product: row block ti (bm rows) covers columns
+// from its diagonal block on, ti*bm + tj*bn for tj = 0, 1, ..., so no tile
+// reaches below the diagonal block of its rows.
+int64_t sym_tiles(int m, int bm, int bn) {
   int64_t t = 0;
-  for (int64_t ti = 0; ti < cdiv(m, kTcBM); ++ti)  // column tiles tj with tj*bn + bn - 1 >= ti*128
-    t += tn - std::min<int64_t>(tn, (ti * kTcBM) / bn);
+  for (int64_t ti = 0; ti < cdiv(m, bm); ++ti) t += cdiv(m - ti * bm, bn);
   return t;
 }
 
-int32_t default_bn_sym(int m) { return kWideTileCost * sym_tiles(m, 256) <= sym_tiles(m, 128) ? 256 : 128; }
+int32_t default_bn_sym(int m) {
+  return kWideTileCost * sym_tiles(m, kTcBM, 256) <= sym_tiles(m, kTcBM, 128) ? 256 : 128;
+}
 int32_t default_bn_gemm(int n) { return kWideTileCost * cdiv(n, 256) <= cdiv(n, 128) ? 256 : 128; }
 
 // Tiles of one phase for one bucket, appended in cost order.
@@ -265,12 +271,11 @@ void add_tiles(const dmuon_plan_s& P, int kind, int bucket_local, const BucketPl
     for (int s = 0; s < B.count; ++s)
       for (int tj = 0; tj < tn; ++tj)
         for (int ti = 0; ti < tm; ++ti) out.push_back(make_int4(bucket_local, s, ti, tj));
-  } else {
-    const int tn = static_cast<int>(cdiv(B.m, BN));
+  } else {  // symmetric products: tile (ti, tj) covers columns ti*BM + tj*BN.. (from the diagonal block on)
     for (int s = 0; s < B.count; ++s)
       for (int ti = 0; ti < tm; ++ti)
-        for (int tj = 0; tj < tn; ++tj)
-          if (tj * BN + BN - 1 >= ti * BM) out.push_back(make_int4(bucket_local, s, ti, tj));
+        for (int tj = 0; tj < static_cast<int>(cdiv(B.m - ti * BM, BN)); ++tj)
+          out.push_back(make_int4(bucket_local, s, ti, tj));
   }
 }
 
@@ -442,15 +447,18 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   if (P.ns_steps > 0) {
     for (const BucketPlan& B : P.buckets) {
       const int64_t tm = cdiv(B.m, P.tile_m), bn = P.tc ? 128 : kSimtBN;
-      int64_t sym = 0;
-      for (int64_t ti = 0; ti < tm; ++ti)
-        for (int64_t tj = 0; tj < cdiv(B.m, bn); ++tj)
-          if (tj * bn + bn - 1 >= ti * P.tile_m) ++sym;
-      cap_items += B.count * (2 * sym + tm * cdiv(B.n, bn));
+      cap_items += B.count * (2 * sym_tiles(B.m, P.tile_m, static_cast<int>(bn)) + tm * cdiv(B.n, bn));
     }
   }
   P.off_items = take((int64_t)sizeof(int4) * std::max<int64_t>(std::max<int64_t>(cap_items, (int64_t)P.items.size()), 1));
   P.off_probe = take((int64_t)sizeof(int4) * kProbeTiles);
+  // per launch of a step (and one for the tuning probes): the tile-claim counter pair, 128 bytes
+  // apart; and the per-CTA profiling records of each launch. The launch count is bounded by the
+  // step's sequence below: 3 + (4 * ns_steps) per chunk at most.
+  const int64_t max_launches = 3 + 4LL * std::max(P.ns_steps, 1) * std::max<int64_t>((int64_t)P.chunks.size(), 1);
+  P.off_sched = take(kSchedBytes * (max_launches + 1));
+  P.off_probe_sched = P.off_sched + kSchedBytes * max_launches;
+  P.off_cta = take(16LL * kMaxCtaRecords * max_launches);
   for (BucketPlan& B : P.buckets) {
     B.off_slotmat = take(4LL * B.count);
     B.x_mat_bytes = (int64_t)B.m * B.x_ld * P.xel;
@@ -739,6 +747,8 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         tp.status = P.sp.status;
         tp.param_bf16 = P.sp.param_bf16;
         tp.timeout_ns = 2000000000LL;
+        tp.sched = (P.flags & DMUON_FLAG_STATIC_TILES) ? nullptr
+                                                        : reinterpret_cast<unsigned*>(P.ws + P.off_probe_sched);
         const int grid = std::max(1, std::min(n, P.num_sms));
         float ms = 0.f;
         if ((e = launch_tc(phase, bns[bi], tp, grid, s)) != cudaSuccess || (e = cudaEventRecord(e0, s)) != cudaSuccess) {
@@ -806,7 +816,7 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES |
-                DMUON_FLAG_EPILOGUE_AX))
+                DMUON_FLAG_EPILOGUE_AX | DMUON_FLAG_STATIC_TILES))
     return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
@@ -918,7 +928,8 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
     return cuda_fail(e, "table upload");
   for (const BucketPlan& B : P->buckets)
     if ((e = up(B.off_slotmat, B.mats.data(), 4 * B.mats.size())) != cudaSuccess) return cuda_fail(e, "upload");
-  if ((e = cudaMemsetAsync(ws + P->off_status, 0, P->off_s - P->off_status, s)) != cudaSuccess)
+  if ((e = cudaMemsetAsync(ws + P->off_status, 0, P->off_s - P->off_status, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(ws + P->off_sched, 0, P->off_cta - P->off_sched, s)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "bind sync");
   if (test_hook("bind_tables")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_tables)");
@@ -994,6 +1005,10 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       tp.status = sp.status;
       tp.param_bf16 = sp.param_bf16;
       tp.timeout_ns = 2000000000LL;
+      const size_t li = static_cast<size_t>(&L - P->launches.data());
+      tp.sched = (L.pair || (P->flags & DMUON_FLAG_STATIC_TILES))
+                     ? nullptr
+                     : reinterpret_cast<unsigned*>(ws + P->off_sched + kSchedBytes * static_cast<int64_t>(li));
       L.grid = L.pair ? std::max(1, std::min(lr.count, P->num_sms / 2)) : std::max(1, std::min(lr.count, P->num_sms));
       L.param_index = static_cast<int>(P->tc_params.size());
       P->tc_params.push_back(tp);
@@ -1162,6 +1177,9 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
       tp.lr = lr;
       tp.ptrs = dptrs;
       tp.wmaps = dwmaps;
+      tp.cta_times = P->cta_times ? reinterpret_cast<unsigned long long*>(P->ws + P->off_cta) +
+                                        2LL * kMaxCtaRecords * static_cast<int64_t>(li)
+                                  : nullptr;
       e = L.pair ? launch_tc_pair(L.phase, tp, L.grid, s) : launch_tc(L.phase, L.bn, tp, L.grid, s);
     } else {
       SimtParams& p = P->simt_params[L.param_index];
@@ -1236,7 +1254,33 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
              B.pair ? "true" : "false", B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2]);
     j += t;
   }
-  j += "], \"lists\": [";
+  j += "], \"regions\": {";
+  // Workspace byte ranges [offset, bytes]: "tables" are written by bind and only read by steps;
+  // "scratch" is written by every step before the step reads it (per-matrix s, partial sums,
+  // the bucket buffers, the update capture); "status" accumulates device status bits.
+  snprintf(t, sizeof t, "\"status\": [%lld, 4], \"tables\": [[%lld, %lld]", (long long)P->off_status,
+           (long long)P->off_mats, (long long)(P->off_probe + (int64_t)sizeof(int4) * kProbeTiles - P->off_mats));
+  j += t;
+  for (const BucketPlan& B : P->buckets) {
+    snprintf(t, sizeof t, ", [%lld, %lld]", (long long)B.off_slotmat, 4LL * B.count);
+    j += t;
+  }
+  snprintf(t, sizeof t, "], \"scratch\": [[%lld, %lld], [%lld, %lld]", (long long)P->off_s, 4LL * (long long)P->mats.size(),
+           (long long)P->off_partial, (long long)(4LL * kPartialsPerUnit * std::max<int64_t>(P->n_units, 1)));
+  j += t;
+  for (const BucketPlan& B : P->buckets)
+    for (int r = 0; r < kBufCount; ++r)
+      if (B.off[r] >= 0) {
+        snprintf(t, sizeof t, ", [%lld, %lld]", (long long)B.off[r],
+                 (long long)((B.is_x(r) ? B.x_mat_bytes : B.a_mat_bytes) * B.count));
+        j += t;
+      }
+  if (P->off_capture >= 0) {
+    snprintf(t, sizeof t, ", [%lld, %lld]", (long long)P->off_capture, 4LL * std::max<int64_t>(P->cap_elems, 1));
+    j += t;
+  }
+  j += "]}";
+  j += ", \"lists\": [";
   for (size_t c = 0; c < P->gram_lists.size(); ++c) {
     snprintf(t, sizeof t, "%s{\"chunk\": %zu, \"gram\": %d, \"poly\": %d, \"gemm\": %d}", c ? ", " : "", c,
              P->gram_lists[c].count, P->poly_lists[c].count, P->gemm_lists[c].count);
@@ -1327,6 +1371,38 @@ dmuon_status dmuon_plan_costs(dmuon_plan_t P, double* per_matrix_ms, int32_t n) 
     per_bucket[b] = (nsym * (n_xx * B.tile_ms[0] + n_mm * B.tile_ms[1]) + ngemm * n_gm * B.tile_ms[2]) / P->num_sms;
   }
   for (size_t i = 0; i < P->mats.size(); ++i) per_matrix_ms[i] = per_bucket[P->mats[i].bucket];
+  return DMUON_OK;
+}
+
+dmuon_status dmuon_profile_cta_times(dmuon_plan_t P, int32_t enable) {
+  if (P == nullptr) return fail(DMUON_ERR_INVALID_ARG, "plan is NULL");
+  P->cta_times = enable != 0;
+  return DMUON_OK;
+}
+
+dmuon_status dmuon_read_cta_times(dmuon_plan_t P, int32_t launch, uint64_t* out, int32_t cap, int32_t* n_ctas,
+                                  void* stream) {
+  if (P == nullptr || n_ctas == nullptr) return fail(DMUON_ERR_INVALID_ARG, "NULL argument");
+  if (P->ws == nullptr) return fail(DMUON_ERR_NOT_BOUND, "plan is not bound");
+  if (launch < 0 || launch >= static_cast<int32_t>(P->launches.size()))
+    return fail(DMUON_ERR_INVALID_ARG, "launch index %d out of range", launch);
+  const Launch& L = P->launches[launch];
+  const bool tc_kind = L.kind == DMUON_KIND_GRAM || L.kind == DMUON_KIND_POLY || L.kind == DMUON_KIND_GEMM ||
+                       L.kind == DMUON_KIND_SYMM;
+  if (!P->tc || !tc_kind || L.pair) {
+    *n_ctas = 0;
+    return DMUON_OK;
+  }
+  const int n = std::min<int>(L.grid, kMaxCtaRecords);
+  *n_ctas = n;
+  if (out == nullptr || cap <= 0) return DMUON_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const size_t bytes = 16ULL * std::min(n, cap);
+  if ((e = cudaMemcpyAsync(out, P->ws + P->off_cta + 16LL * kMaxCtaRecords * launch, bytes, cudaMemcpyDeviceToHost,
+                           s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess)
+    return cuda_fail(e, "per-CTA times copy");
   return DMUON_OK;
 }
 

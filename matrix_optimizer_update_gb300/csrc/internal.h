@@ -99,7 +99,14 @@ struct TcParams {
   unsigned* status;
   int32_t param_bf16;
   int64_t timeout_ns;
+  // Dynamic tile claiming (one-SM kernel): [0] counts claimed items, [1] CTAs that finished;
+  // both zero before the launch, and the last CTA leaves them zero. nullptr = CTA b takes items
+  // b, b + grid, ... (the two-SM kernel always does).
+  unsigned* sched;
+  unsigned long long* cta_times;  // profiling: start and end (global timer, ns) per CTA, or nullptr
 };
+
+constexpr int kMaxCtaRecords = 1024;  // CTAs per launch the per-CTA profiling records
 
 // One bucket as seen by a fp32 SIMT launch.
 struct SimtBucket {

@@ -20,7 +20,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
   const int4 it = p.items[blockIdx.x];
   const SimtBucket& B = p.bk[it.x];
   const int slot = it.y;
-  const int row0 = it.z * kSimtBM, col0 = it.w * kSimtBN;
+  // symmetric products list their tiles from the diagonal block on: column tile it.w counts from it.z
+  const int row0 = it.z * kSimtBM, col0 = (PHASE == kPhaseGemm) ? it.w * kSimtBN : row0 + it.w * kSimtBN;
   const float* opA = B.opA + slot * B.a_mat_stride;
   const float* opB = B.opB + slot * B.b_mat_stride;
   const int tid = threadIdx.x;

@@ -67,6 +67,10 @@ struct TcCfg {
   static constexpr int kEpiChunks = BN / 2 / 32;       // 32-column chunks per epilogue warp
 };
 
+// Tiles claimed by the TMA thread reach the MMA thread and the epilogue warps
+// through a ring of this many item indices.
+constexpr int kSchedDepth = 8;
+
 template <int STAGES>
 struct TcShared {
   uint64_t full[STAGES];
@@ -74,11 +78,32 @@ struct TcShared {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
+  uint64_t sched_full[kSchedDepth];   // item published (1 arrival: the TMA thread)
+  uint64_t sched_empty[kSchedDepth];  // item read by the MMA thread and every epilogue warp
+  int ring[kSchedDepth];              // item index, -1 = no more tiles
   uint32_t tmem_base;
   int abort_flag;
 };
 
 static_assert(sizeof(TcShared<6>) <= 1024, "barriers must fit their 1 KB");
+
+// Consumer side of the item ring: the j-th item of this CTA (false when the CTA gives up).
+template <int STAGES>
+__device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int& w, volatile int* abortf,
+                                          const TcParams& p) {
+  const uint32_t slot = j % kSchedDepth;
+  if (!ptx::mbar_wait(&sh->sched_full[slot], (j / kSchedDepth) & 1u, abortf, p.status, p.timeout_ns)) return false;
+  w = *reinterpret_cast<volatile int*>(&sh->ring[slot]);
+  ptx::mbar_arrive(&sh->sched_empty[slot]);
+  return true;
+}
+
+// First output column of a symmetric-product tile (bucket, slot, ti, tj):
+// the planner lists each row block's tiles from its diagonal block on.
+template <int BN>
+__device__ __forceinline__ int sym_col0(const int4& it) {
+  return it.z * kTcBM + it.w * BN;
+}
 
 template <int PHASE, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_constant__ TcParams p) {
@@ -109,6 +134,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       ptx::mbar_init(&sh->tempty[a], kEpiWarps);
     }
     ptx::mbar_init(&sh->mma_done, 1);
+    for (int k = 0; k < kSchedDepth; ++k) {
+      ptx::mbar_init(&sh->sched_full[k], 1);
+      ptx::mbar_init(&sh->sched_empty[k], 1 + kEpiWarps);
+    }
     sh->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -121,13 +150,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   ptx::tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
 
+  const uint64_t t_start = ptx::globaltimer();
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      uint32_t stage = 0, phase = 0;
+      // Also the tile scheduler: with p.sched, tiles are claimed from the launch's counter in
+      // list order (largest cost first) as this CTA gets to them, one claim ahead of the loads;
+      // without it, CTA b takes items b, b + grid, b + 2*grid, ... Either way each claimed item
+      // goes into the ring for the MMA thread and the epilogue warps; -1 ends the list.
+      auto claim = [&](uint32_t j) -> int {
+        if (p.sched == nullptr) {
+          const int64_t w = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+          return w < p.n_items ? static_cast<int>(w) : -1;
+        }
+        const unsigned w = atomicAdd(p.sched, 1u);
+        return w < static_cast<unsigned>(p.n_items) ? static_cast<int>(w) : -1;
+      };
+      uint32_t stage = 0, phase = 0, j = 0;
       uint32_t issued[kTcStages];
       for (int s = 0; s < kTcStages; ++s) issued[s] = 0;
-      for (int w = blockIdx.x; w < p.n_items; w += gridDim.x) {
+      int w = claim(0);
+      for (;;) {
+        const uint32_t slot = j % kSchedDepth;
+        if (!ptx::mbar_wait(&sh->sched_empty[slot], ((j / kSchedDepth) & 1u) ^ 1u, abortf, p.status, p.timeout_ns))
+          break;
+        sh->ring[slot] = w;
+        ptx::mbar_arrive(&sh->sched_full[slot]);
+        ++j;
+        if (w < 0) break;
+        const int next = claim(j);  // its latency hides under this tile's loads
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
@@ -145,8 +197,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
             for (int q = 0; q < BN / 64; ++q)
               ptx::tma_load_3d(sB + stage * kStageB + q * (64 * kTcBK * 2), &B.tmB, &sh->full[stage],
                                it.w * BN + q * 64, k0, it.y);
-          } else {
-            ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, it.w * BN, it.y);
+          } else {  // rows of the tile's columns; rows past the matrix's edge are zero-filled
+            ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, sym_col0<BN>(it), it.y);
           }
           ++issued[stage];
           if (++stage == kTcStages) {
@@ -155,6 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           }
         }
         if (!ok) break;
+        w = next;
       }
       // Every issued copy must land before the CTA may exit (matters only after an abort).
       for (int s = 0; s < kTcStages; ++s) {
@@ -167,14 +220,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16(kTcBM, BN, PHASE == kPhaseGemm);
+      constexpr uint32_t idesc_full = ptx::idesc_bf16(kTcBM, BN, PHASE == kPhaseGemm);
+      constexpr uint32_t idesc_half = ptx::idesc_bf16(kTcBM, BN / 2, PHASE == kPhaseGemm);
       uint32_t stage = 0, phase = 0, local = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      for (int w; ok && ring_take(sh, local, w, abortf, p) && w >= 0; ++local) {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         const uint32_t acc = local & 1u;
+        // A symmetric tile whose right half lies wholly past the matrix's edge multiplies only its
+        // left half (the first BN/2 rows of the B stage); the epilogue stores nothing of the rest.
+        const uint32_t idesc =
+            (PHASE != kPhaseGemm && BN == 256 && sym_col0<BN>(it) + BN / 2 >= B.m) ? idesc_half : idesc_full;
         if (!ptx::mbar_wait(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + acc * BN;
@@ -222,12 +280,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     const int half = (warp - 2) >> 2;
     uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
     uint32_t local = 0, nbox = 0;
-    for (int w = blockIdx.x; w < p.n_items; w += gridDim.x, ++local) {
+    for (;; ++local) {
+      int w = -2;  // -2: the CTA gave up
+      if (lane == 0 && !ring_take(sh, local, w, abortf, p)) w = -2;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) break;
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
       const int i0 = it.z * kTcBM + q * 32;
-      const int jbase = it.w * BN + half * (BN / 2);
+      const int jbase = (PHASE == kPhaseGemm ? it.w * BN : sym_col0<BN>(it)) + half * (BN / 2);
       const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
       const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
         return ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);
@@ -242,6 +304,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
   }
 
   __syncthreads();
+  if (threadIdx.x == 0) {
+    if (p.cta_times != nullptr) {  // profiling: this CTA's start and end on the global timer
+      p.cta_times[2 * blockIdx.x] = t_start;
+      p.cta_times[2 * blockIdx.x + 1] = ptx::globaltimer();
+    }
+    if (p.sched != nullptr) {
+      // Every claim of this CTA precedes its arrival here; the last CTA to arrive leaves both
+      // words at zero for the next launch that uses them.
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        p.sched[0] = 0u;
+        p.sched[1] = 0u;
+      }
+    }
+  }
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();

@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
             for (int q = 0; q < 2; ++q)
               ptx::tma_load_3d_pair(sB + stage * kHalfB + q * (64 * kTcBK * 2), &B.tmB, fb,
                                     it.w * kPairBN + rank * 128 + q * 64, k0, it.y);
-          } else {
-            ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, it.w * kPairBN + rank * 128, it.y);
+          } else {  // symmetric products list a row pair's tiles from its diagonal block on
+            ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, (it.z + it.w) * kPairBN + rank * 128, it.y);
           }
           ++issued[stage];
           if (++stage == kStages) {
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
       const int i0 = it.z * kPairBM + static_cast<int>(rank) * 128 + q * 32;
-      const int jbase = it.w * kPairBN + half * (kPairBN / 2);
+      const int jbase = (PHASE == kPhaseGemm ? it.w : it.z + it.w) * kPairBN + half * (kPairBN / 2);
       const uint32_t tbase = tmem + acc * kPairBN + half * (kPairBN / 2) + ((uint32_t)(q * 32) << 16);
       const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
         return ptx::mbar_wait_cluster(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);

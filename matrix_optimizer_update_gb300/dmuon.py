@@ -35,6 +35,7 @@ FLAG_GRAM_NS = 0x2
 FLAG_TUNE = 0x4
 FLAG_PAIR_TILES = 0x8
 FLAG_EPILOGUE_AX = 0x10
+FLAG_STATIC_TILES = 0x20
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 
@@ -45,7 +46,8 @@ KIND_NAMES = {0: "momentum", 1: "gram", 2: "poly", 3: "gemm", 4: "update0", 5: "
 EXPORTS = (
     "dmuon_plan", "dmuon_plan_workspace_bytes", "dmuon_plan_bind", "dmuon_step",
     "dmuon_set_weight_events", "dmuon_read_device_status", "dmuon_read_update", "dmuon_plan_describe",
-    "dmuon_profile_begin", "dmuon_profile_end", "dmuon_plan_costs", "dmuon_launch_count",
+    "dmuon_profile_begin", "dmuon_profile_end", "dmuon_profile_cta_times", "dmuon_read_cta_times",
+    "dmuon_plan_costs", "dmuon_launch_count",
     "dmuon_selftest_wait_timeout", "dmuon_momentum_norm_noalloc", "dmuon_assign_owners", "dmuon_adamw_flat",
     "dmuon_plan_destroy", "dmuon_last_error", "dmuon_version",
 )
@@ -92,6 +94,8 @@ def lib():
         "dmuon_profile_begin": (i32, [vp, i32]),
         "dmuon_profile_end": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(f32), ctypes.POINTER(ctypes.c_double),
                                     i32, ctypes.POINTER(i32)]),
+        "dmuon_profile_cta_times": (i32, [vp, i32]),
+        "dmuon_read_cta_times": (i32, [vp, i32, ctypes.POINTER(ctypes.c_uint64), i32, ctypes.POINTER(i32), vp]),
         "dmuon_plan_costs": (i32, [vp, ctypes.POINTER(ctypes.c_double), i32]),
         "dmuon_launch_count": (i32, [vp, ctypes.POINTER(i64)]),
         "dmuon_selftest_wait_timeout": (i32, [vp, i64, vp, ctypes.POINTER(u32)]),
@@ -209,6 +213,19 @@ class Plan:
         _check(lib().dmuon_profile_end(self._h, kinds, ms, work, cap, ctypes.byref(n)))
         k = min(n.value, cap)
         return [(kinds[i], ms[i], work[i]) for i in range(k)]
+
+    def profile_cta_times(self, enable: bool = True):
+        _check(lib().dmuon_profile_cta_times(self._h, int(bool(enable))))
+
+    def read_cta_times(self, launch: int, stream: int = 0):
+        """[(start_ns, end_ns)] per CTA of launch `launch` of the last recorded step."""
+        n = ctypes.c_int32()
+        _check(lib().dmuon_read_cta_times(self._h, launch, None, 0, ctypes.byref(n), ctypes.c_void_p(stream)))
+        if n.value == 0:
+            return []
+        buf = (ctypes.c_uint64 * (2 * n.value))()
+        _check(lib().dmuon_read_cta_times(self._h, launch, buf, n.value, ctypes.byref(n), ctypes.c_void_p(stream)))
+        return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
 
     def costs(self):
         """Measured per-matrix cost (ms) of a tuned plan."""

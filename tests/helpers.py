@@ -61,7 +61,7 @@ class LibRun:
     """Flat device buffers for one batch plus a bound plan."""
 
     def __init__(self, shapes, *, param="bf16", grad="bf16", compute="bf16", ns_steps=5, coeffs=ref.DEFAULT_COEFFS,
-                 eps=1e-7, capture=True, device="cuda", gram_ns=False, pair=False, epilogue_ax=False):
+                 eps=1e-7, capture=True, device="cuda", gram_ns=False, pair=False, epilogue_ax=False, flags=0):
         self.shapes = list(shapes)
         self.param, self.grad, self.compute = param, grad, compute
         self.offs, total = layout(self.shapes)
@@ -71,7 +71,8 @@ class LibRun:
         self.muon = dm.Muon.create(self.shapes, ns_steps=ns_steps, coeffs=coeffs, eps=eps, param=param, grad=grad,
                                    compute=compute, device=device,
                                    flags=(dm.FLAG_CAPTURE_UPDATE if capture else 0) | (dm.FLAG_GRAM_NS if gram_ns else 0)
-                                   | (dm.FLAG_PAIR_TILES if pair else 0) | (dm.FLAG_EPILOGUE_AX if epilogue_ax else 0))
+                                   | (dm.FLAG_PAIR_TILES if pair else 0) | (dm.FLAG_EPILOGUE_AX if epilogue_ax else 0)
+                                   | flags)
         self.capture = capture
 
     def view(self, flat, i):

@@ -106,7 +106,9 @@ def cdiv(a, b):
 
 
 def brute_tiles(m, n, bm, bn_sym, bn_gemm):
-    gram = sum(1 for ti in range(cdiv(m, bm)) for tj in range(cdiv(m, bn_sym)) if tj * bn_sym + bn_sym - 1 >= ti * bm)
+    # symmetric products: row block ti's tiles start at its diagonal block, columns ti*bm + tj*bn_sym..,
+    # as long as they start inside the matrix
+    gram = sum(1 for ti in range(cdiv(m, bm)) for tj in range(cdiv(m, bn_sym)) if ti * bm + tj * bn_sym < m)
     gemm = cdiv(m, bm) * cdiv(n, bn_gemm)
     return gram, gemm
 

@@ -310,12 +310,14 @@ def test_weight_sets_replaced_store_through_their_own_maps():
             assert torch.equal(a.view(Ms[k], i), a.view(Mb[k], i)), (k, i)
 
 
-@pytest.mark.parametrize("flags", ["standard", "gram", "pair"])
+@pytest.mark.parametrize("flags", ["standard", "gram", "pair", "static"])
 def test_cuda_graph_replay_matches_eager(flags):
     # after one uncaptured step with the same pointers, dmuon_step records no host copies and can be
-    # captured; two graph replays must equal two eager steps bit for bit
+    # captured; two graph replays must equal two eager steps bit for bit (the tile-claim counters
+    # of each launch are left at zero by the launch itself, so replays claim from zero again)
     shapes = [(512, 1024), (1024, 512), (256, 256)]
-    kw = {"gram_ns": flags == "gram", "pair": flags == "pair", "capture": False}
+    kw = {"gram_ns": flags == "gram", "pair": flags == "pair", "capture": False,
+          "flags": dm.FLAG_STATIC_TILES if flags == "static" else 0}
     a = LibRun(shapes, **kw)
     _fill(a, 6000, m_std=1e-3)
     W0, M0 = a.W.clone(), a.M.clone()
