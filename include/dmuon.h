@@ -53,7 +53,8 @@ typedef enum {
   DMUON_ERR_WORKSPACE = -3,   /* workspace NULL, too small or misaligned       */
   DMUON_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed             */
   DMUON_ERR_NOT_BOUND = -5,   /* dmuon_step before dmuon_plan_bind             */
-  DMUON_ERR_DEVICE = -6       /* a device status bit is set (see below)        */
+  DMUON_ERR_DEVICE = -6       /* a device-side result is wrong: a status bit is
+                                 set, or a DMUON_FLAG_DEBUG_CHECKS check failed */
 } dmuon_status;
 
 typedef enum { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
@@ -113,10 +114,33 @@ typedef struct {
                                           claim the next tile from the launch's counter
                                           as it becomes free. Same results bit for bit;
                                           kept to compare the two schedules.       */
-#define DMUON_FLAG_TUNE 0x4u           /* at bind, time both tile widths (128, 256)
-                                          per bucket on the bound workspace, keep
-                                          the faster, and order tiles by measured
-                                          time (see dmuon_plan_costs). bf16 only. */
+#define DMUON_FLAG_DEBUG_CHECKS 0x40u /* debugging aid: after every launch of a step
+                                          the host waits for it, copies back the
+                                          operands of a few sampled output elements
+                                          (momentum, U, s, product elements, one on
+                                          the diagonal, one mirror, updated weights)
+                                          and recomputes them in double precision;
+                                          dmuon_step returns DMUON_ERR_DEVICE, with
+                                          the launch, matrix and element in
+                                          dmuon_last_error(), when one is off by more
+                                          than its rounding allows. Makes every step
+                                          synchronous and slow; not for capture.
+                                          Test hook: with the environment variable
+                                          DMUON_TEST_SKIP_LAUNCH=<i>, launch i of
+                                          each step is left out, so its outputs are
+                                          stale and the checks must report them.  */
+#define DMUON_FLAG_TUNE 0x4u           /* at bind, time three tile configurations per
+                                          bucket on the bound workspace (one-SM
+                                          128 x 128 and 128 x 256 tiles, two-SM
+                                          256 x 256 pairs where the short side is
+                                          >= 256; each with its ring depth), keep
+                                          the cheapest, and order tiles by measured
+                                          time (see dmuon_plan_costs). Timings are
+                                          cached for the process by (short side,
+                                          long side, weight dtype, SM count,
+                                          compute capability): a later plan with
+                                          the same shapes binds without timing.
+                                          bf16 only.                              */
 
 /* Device status bits (dmuon_read_device_status). */
 #define DMUON_DEV_NONFINITE_NORM 0x1u  /* ||U||_F was NaN or Inf for some matrix  */

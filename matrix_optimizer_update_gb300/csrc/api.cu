@@ -23,6 +23,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <tuple>
 #include <string>
 #include <vector>
@@ -102,6 +103,14 @@ bool test_hook(const char* where) {
   return v != nullptr && std::strcmp(v, where) == 0;
 }
 
+// Test hook of the debug checks: DMUON_TEST_SKIP_LAUNCH=<i> leaves launch i of
+// every step out (only under DMUON_FLAG_DEBUG_CHECKS), so that its outputs are
+// stale and the checks must report them.
+bool test_skip_launch(int li) {
+  const char* v = std::getenv("DMUON_TEST_SKIP_LAUNCH");
+  return v != nullptr && v[0] != '\0' && std::atoi(v) == li;
+}
+
 // Workspace buffers of a bucket, by role. Standard buckets use X0/X1 (the
 // iterate, ping-pong), A and B; Gram-space buckets use X0 (U, read twice), G,
 // P, Q0/Q1 (ping-pong) and R.
@@ -114,7 +123,9 @@ struct BucketPlan {
   bool pair = false;          // 256 x 256 tiles on CTA pairs (two-SM UMMA)
   int32_t bn_sym = 0;         // tile width of the symmetric products (m x m outputs)
   int32_t bn_gemm = 0;        // tile width of the m x n product
-  double tile_ms[3] = {0, 0, 0};  // measured ms per tile: X X^T (K = n), m x m products, gemm; 0 = not measured
+  // measured SM-ms per tile (time per tile x SMs it occupies): X X^T (K = n), m x m products, gemm;
+  // 0 = not measured
+  double tile_ms[3] = {0, 0, 0};
   std::vector<int32_t> mats;  // slot -> global matrix index
   int64_t off_slotmat = -1;
   int64_t off[kBufCount] = {-1, -1, -1, -1, -1, -1, -1};
@@ -216,6 +227,7 @@ struct dmuon_plan_s {
   int64_t launch_count = 0;
   int64_t steps_taken = 0;
   bool tuned = false;
+  int tune_timed = 0, tune_cached = 0;  // buckets timed at bind / taken from the tuning cache
   bool cta_times = false;  // dmuon_profile_cta_times: record per-CTA start/end of tensor-core launches
   // ---- ordering of the weight writes against other streams (dmuon_set_weight_events)
   cudaEvent_t w_wait = nullptr;   // waited on before the first launch that writes W
@@ -690,14 +702,36 @@ void destroy_events(dmuon_plan_s& P) {
   P.prof_max = P.prof_n = 0;
 }
 
-// Init-time tuning (DMUON_FLAG_TUNE): for every bucket and both tile widths,
-// time a GPU-filling slice of its X X^T tiles (K = n), of its m x m products
-// (K = m) and of its gemm tiles on the bound workspace (results discarded),
-// keep the faster width per kind of product, and record the measured time per
-// tile, which then orders the tile lists and feeds dmuon_plan_costs. This is
-// the single-GPU form of the pages' initialisation profiling of kernel
-// schedules per matrix shape (gist.science summary section 2.3, "Profiling";
-// section 2.4: the chosen configuration is cached and reused).
+// Init-time tuning (DMUON_FLAG_TUNE): for every bucket and every tile
+// configuration (one-SM 128 x 128 tiles with a 6-stage ring, one-SM 128 x 256
+// with 4 stages, and, where the short side is at least 256, two-SM 256 x 256
+// pairs with 6 stages), time a GPU-filling slice of its X X^T tiles (K = n),
+// of its m x m products (K = m) and of its gemm tiles on the bound workspace
+// (results discarded), keep the cheapest configuration per bucket, and record
+// the measured SM-time per tile, which then orders the tile lists and feeds
+// dmuon_plan_costs. The per-tile times are kept in a process-wide cache keyed
+// by (short side, long side, weight dtype, SM count, compute capability), so
+// later plans with the same shapes bind without timing again. This is the
+// single-GPU form of the pages' initialisation profiling of kernel schedules
+// per matrix shape ("DMuon: Efficient Distributed Muon Training with
+// Near-Adam Overhead", gist.science summary section 2.3, "Profiling";
+// section 2.4: tile shapes, block sizes and pipeline depths are searched and
+// the chosen configuration is cached and reused).
+constexpr int kTuneCands = 3;  // 0: one-SM 128 wide, 1: one-SM 256 wide, 2: two-SM 256 x 256
+constexpr int kTuneCandBn[kTuneCands] = {128, 256, 256};
+
+struct TuneKey {
+  int m, n, param, sms, cc;
+  bool operator<(const TuneKey& o) const {
+    return std::tie(m, n, param, sms, cc) < std::tie(o.m, o.n, o.param, o.sms, o.cc);
+  }
+};
+struct TuneTimes {
+  double sm_ms[kTuneCands][3];  // SM-ms per tile: X X^T, m x m product, gemm; 0 = candidate not timed
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, TuneTimes> g_tune_cache;
+
 dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   cudaError_t e;
@@ -705,22 +739,35 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
     if (e0) cudaEventDestroy(e0);
     return cuda_fail(e, "cudaEventCreate");
   }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, P.device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, P.device);
   dmuon_status st = DMUON_OK;
   int4* probe = reinterpret_cast<int4*>(P.ws + P.off_probe);
   std::vector<int4> tiles;
-  const int bns[2] = {128, 256};
+  P.tune_timed = P.tune_cached = 0;
   for (BucketPlan& B : P.buckets) {
-    double tms[2][3] = {{0, 0, 0}, {0, 0, 0}};
-    int64_t per_mat[2][2] = {{0, 0}, {0, 0}};
-    for (int bi = 0; bi < 2 && st == DMUON_OK; ++bi) {
+    const TuneKey key{B.m, B.n, P.dt.param, P.num_sms, 10 * major + minor};
+    TuneTimes tt{};
+    bool cached = false;
+    {
+      std::lock_guard<std::mutex> lock(g_tune_mu);
+      auto it = g_tune_cache.find(key);
+      if (it != g_tune_cache.end()) {
+        tt = it->second;
+        cached = true;
+      }
+    }
+    for (int ci = 0; ci < kTuneCands && st == DMUON_OK && !cached; ++ci) {
       BucketPlan T = B;
-      T.bn_sym = T.bn_gemm = bns[bi];
-      T.pair = false;  // the probes time one-SM tiles
+      T.bn_sym = T.bn_gemm = kTuneCandBn[ci];
+      T.pair = (ci == 2);
+      if (T.pair && B.m < 256) continue;  // a pair tile would be mostly empty
       for (int kind = 0; kind < 3 && st == DMUON_OK; ++kind) {
         tiles.clear();
         add_tiles(P, kind == 2 ? DMUON_KIND_GEMM : DMUON_KIND_GRAM, 0, T, tiles);
-        per_mat[bi][kind == 2 ? 1 : 0] = static_cast<int64_t>(tiles.size()) / B.count;
-        const int n = static_cast<int>(std::min<int64_t>({(int64_t)tiles.size(), 4LL * P.num_sms, kProbeTiles}));
+        const int slots = T.pair ? P.num_sms / 2 : P.num_sms;
+        const int n = static_cast<int>(std::min<int64_t>({(int64_t)tiles.size(), 4LL * slots, kProbeTiles}));
         if ((e = cudaMemcpyAsync(probe, tiles.data(), sizeof(int4) * n, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
             (e = cudaStreamSynchronize(s)) != cudaSuccess) {
           st = cuda_fail(e, "probe upload");
@@ -737,7 +784,9 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         }
         TcParams tp;
         std::memset(&tp, 0, sizeof(tp));
-        if ((st = fill_tc_bucket(P, T, phase, bns[bi], opA, opB, out, aux, tp.bk[0])) != DMUON_OK) break;
+        // a pair's CTAs each load 128 rows of a K-major B operand
+        if ((st = fill_tc_bucket(P, T, phase, T.pair ? 128 : T.bn_sym, opA, opB, out, aux, tp.bk[0])) != DMUON_OK)
+          break;
         tp.items = probe;
         tp.n_items = n;
         tp.a = 1.f;
@@ -747,15 +796,19 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         tp.status = P.sp.status;
         tp.param_bf16 = P.sp.param_bf16;
         tp.timeout_ns = 2000000000LL;
-        tp.sched = (P.flags & DMUON_FLAG_STATIC_TILES) ? nullptr
-                                                        : reinterpret_cast<unsigned*>(P.ws + P.off_probe_sched);
-        const int grid = std::max(1, std::min(n, P.num_sms));
+        tp.sched = (P.flags & DMUON_FLAG_STATIC_TILES) || T.pair
+                       ? nullptr
+                       : reinterpret_cast<unsigned*>(P.ws + P.off_probe_sched);
+        const int grid = std::max(1, std::min(n, slots));
+        auto launch = [&]() {
+          return T.pair ? launch_tc_pair(phase, tp, grid, s) : launch_tc(phase, T.bn_sym, tp, grid, s);
+        };
         float ms = 0.f;
-        if ((e = launch_tc(phase, bns[bi], tp, grid, s)) != cudaSuccess || (e = cudaEventRecord(e0, s)) != cudaSuccess) {
+        if ((e = launch()) != cudaSuccess || (e = cudaEventRecord(e0, s)) != cudaSuccess) {
           st = cuda_fail(e, "tuning launch");
           break;
         }
-        for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) e = launch_tc(phase, bns[bi], tp, grid, s);
+        for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) e = launch();
         if (e == cudaSuccess) e = cudaEventRecord(e1, s);
         if (e == cudaSuccess) e = cudaEventSynchronize(e1);
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
@@ -764,32 +817,316 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
           break;
         }
         const int waves = (n + grid - 1) / grid;
-        tms[bi][kind] = ms / 3.0 / waves;
+        tt.sm_ms[ci][kind] = ms / 3.0 / waves * (T.pair ? 2.0 : 1.0);  // SMs a tile occupies
       }
     }
     if (st != DMUON_OK) break;
+    if (cached) {
+      ++P.tune_cached;
+    } else {
+      ++P.tune_timed;
+      std::lock_guard<std::mutex> lock(g_tune_mu);
+      g_tune_cache[key] = tt;
+    }
+    // cost per matrix of each configuration: tiles x SM-ms per tile, for the products this bucket's
+    // form runs (the Gram-space form: one X X^T, 4S - 3 m x m products, one gemm)
     const double S = P.ns_steps;
     const double n_xx = B.gram ? 1.0 : S, n_mm = B.gram ? 4.0 * S - 3.0 : S, n_gm = B.gram ? 1.0 : S;
-    int bs = 1, bg = 1;
-    double best_s = 1e300, best_g = 1e300;
-    for (int bi = 0; bi < 2; ++bi) {
-      const double cs = per_mat[bi][0] * (n_xx * tms[bi][0] + n_mm * tms[bi][1]);
-      const double cg = per_mat[bi][1] * n_gm * tms[bi][2];
-      if (cs < best_s) best_s = cs, bs = bi;
-      if (cg < best_g) best_g = cg, bg = bi;
+    double cs[kTuneCands], cg[kTuneCands];
+    for (int ci = 0; ci < kTuneCands; ++ci) {
+      BucketPlan T = B;
+      T.bn_sym = T.bn_gemm = kTuneCandBn[ci];
+      T.pair = (ci == 2);
+      T.count = 1;
+      cs[ci] = cg[ci] = 1e300;
+      if (tt.sm_ms[ci][0] <= 0 || tt.sm_ms[ci][1] <= 0 || tt.sm_ms[ci][2] <= 0) continue;
+      tiles.clear();
+      add_tiles(P, DMUON_KIND_GRAM, 0, T, tiles);
+      cs[ci] = tiles.size() * (n_xx * tt.sm_ms[ci][0] + n_mm * tt.sm_ms[ci][1]);
+      tiles.clear();
+      add_tiles(P, DMUON_KIND_GEMM, 0, T, tiles);
+      cg[ci] = tiles.size() * n_gm * tt.sm_ms[ci][2];
     }
-    B.bn_sym = bns[bs];
-    B.bn_gemm = bns[bg];
-    if (B.pair && (B.bn_sym != 256 || B.bn_gemm != 256)) B.pair = false;  // pairs run 256-wide tiles only
-    B.tile_ms[0] = tms[bs][0];
-    B.tile_ms[1] = tms[bs][1];
-    B.tile_ms[2] = tms[bg][2];
+    const int bs = cs[0] <= cs[1] ? 0 : 1, bg = cg[0] <= cg[1] ? 0 : 1;  // best one-SM widths
+    if (cs[2] + cg[2] < cs[bs] + cg[bg]) {
+      B.pair = true;
+      B.bn_sym = B.bn_gemm = 256;
+      for (int k = 0; k < 3; ++k) B.tile_ms[k] = tt.sm_ms[2][k];
+    } else {
+      B.pair = false;
+      B.bn_sym = kTuneCandBn[bs];
+      B.bn_gemm = kTuneCandBn[bg];
+      B.tile_ms[0] = tt.sm_ms[bs][0];
+      B.tile_ms[1] = tt.sm_ms[bs][1];
+      B.tile_ms[2] = tt.sm_ms[bg][2];
+    }
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
   if (st != DMUON_OK) return st;
   P.tuned = true;
   return finish_plan(P);
+}
+
+// ------------------------------------------------------------------ debug checks
+// DMUON_FLAG_DEBUG_CHECKS: after every launch of a step the host waits for it,
+// copies back the operands of a few sampled output elements and recomputes
+// them in double precision; the step fails with DMUON_ERR_DEVICE and a message
+// naming the launch, the matrix and the element when one is off by more than
+// the rounding of the stored result allows. Sampled per launch: the momentum
+// and U of two elements of three matrices; s of the smallest matrix; for each
+// product two random elements, one diagonal element and, for the symmetric
+// products, the mirror of a random element (which must be bit-identical); for
+// the last product, the updated weights of its samples.
+
+struct DbgRng {
+  uint64_t s;
+  uint32_t next() {
+    s = s * 6364136223846793005ULL + 1442695040888963407ULL;
+    return static_cast<uint32_t>(s >> 33);
+  }
+  int below(int n) { return n > 0 ? static_cast<int>(next() % static_cast<uint32_t>(n)) : 0; }
+};
+
+double decode(const unsigned char* p, int el) {
+  if (el == 2) {
+    uint16_t h;
+    std::memcpy(&h, p, 2);
+    const uint32_t w = static_cast<uint32_t>(h) << 16;
+    float f;
+    std::memcpy(&f, &w, 4);
+    return f;
+  }
+  float f;
+  std::memcpy(&f, p, 4);
+  return f;
+}
+
+// count elements of `el` bytes starting at dptr, stride_el elements apart, into out (as doubles).
+dmuon_status dbg_read(const char* dptr, int64_t count, int el, int64_t stride_el, std::vector<double>& out,
+                      cudaStream_t s) {
+  std::vector<unsigned char> h(static_cast<size_t>(count) * el);
+  cudaError_t e = stride_el == 1
+                      ? cudaMemcpyAsync(h.data(), dptr, h.size(), cudaMemcpyDeviceToHost, s)
+                      : cudaMemcpy2DAsync(h.data(), el, dptr, static_cast<size_t>(stride_el) * el, el, count,
+                                          cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "debug-check copy");
+  out.resize(count);
+  for (int64_t k = 0; k < count; ++k) out[k] = decode(h.data() + k * el, el);
+  return DMUON_OK;
+}
+
+double dbg_one(const char* dptr, int el, cudaStream_t s, dmuon_status& st) {
+  std::vector<double> v;
+  st = dbg_read(dptr, 1, el, 1, v, s);
+  return st == DMUON_OK ? v[0] : 0.0;
+}
+
+// True when got differs from want by more than tol, or is not finite while want is (a non-finite
+// want cannot be checked: it comes from non-finite inputs, which the kernels propagate).
+bool off_by(double got, double want, double tol) {
+  return std::isfinite(want) && !(std::fabs(got - want) <= tol);
+}
+
+struct DbgSample {
+  int bucket = 0, slot = 0, gm = 0, i = 0, j = 0;
+  int64_t w_off = 0;  // element offset of W(i, j) or of the sampled element (momentum pass)
+  double pre_w = 0, pre_g = 0, pre_m = 0;
+  bool mirror = false;  // symmetric products: (i, j) is checked against its mirror (j, i)
+};
+
+double ulp_of(double x, int el) {
+  const int bits = el == 2 ? 8 : 24;
+  const double ax = std::max(std::fabs(x), 1e-38);
+  return std::ldexp(1.0, static_cast<int>(std::floor(std::log2(ax))) - (bits - 1));
+}
+
+dmuon_status dbg_mismatch(const dmuon_plan_s& P, int li, const Launch& L, const DbgSample& x, const char* what,
+                          double got, double want, double tol) {
+  return fail(DMUON_ERR_DEVICE,
+              "debug check: launch %d (kind %d, step %d) matrix %d (%d x %d) %s at (%d, %d): got %.9g, expected "
+              "%.9g (tolerance %.3g)",
+              li, L.kind, L.step, x.gm, P.mats[x.gm].rows, P.mats[x.gm].cols, what, x.i, x.j, got, want, tol);
+}
+
+dmuon_status debug_before(dmuon_plan_s& P, const Launch& L, int li, void* const* params, const void* const* grads,
+                          void* const* momenta, std::vector<DbgSample>& smp, cudaStream_t s) {
+  smp.clear();
+  DbgRng rng{0x9E3779B97F4A7C15ULL ^ (static_cast<uint64_t>(P.steps_taken) << 20) ^ static_cast<uint64_t>(li)};
+  dmuon_status st = DMUON_OK;
+  const int gb = dtype_bytes(P.dt.grad), pb = dtype_bytes(P.dt.param);
+  if (L.kind == DMUON_KIND_MOMENTUM) {
+    const int n = static_cast<int>(P.mats.size());
+    const int picks[3] = {0, n - 1, rng.below(n)};
+    for (int gm : picks)
+      for (int e = 0; e < 2; ++e) {
+        DbgSample x;
+        x.gm = gm;
+        x.i = rng.below(P.mats[gm].rows);
+        x.j = rng.below(P.mats[gm].cols);
+        x.w_off = static_cast<int64_t>(x.i) * P.mats[gm].cols + x.j;
+        x.pre_g = dbg_one(static_cast<const char*>(grads[gm]) + x.w_off * gb, gb, s, st);
+        if (st == DMUON_OK) x.pre_m = dbg_one(static_cast<const char*>(momenta[gm]) + x.w_off * 4, 4, s, st);
+        if (st != DMUON_OK) return st;
+        smp.push_back(x);
+      }
+    return DMUON_OK;
+  }
+  if (L.kind == DMUON_KIND_NORM || L.kind == DMUON_KIND_UPDATE0) {
+    // the smallest matrix: its s (norm) or every weight of one row (update)
+    int best = 0;
+    for (size_t k = 1; k < P.mats.size(); ++k)
+      if ((int64_t)P.mats[k].rows * P.mats[k].cols < (int64_t)P.mats[best].rows * P.mats[best].cols) best = (int)k;
+    DbgSample x;
+    x.gm = best;
+    x.i = rng.below(P.mats[best].rows);
+    x.j = rng.below(P.mats[best].cols);
+    x.w_off = static_cast<int64_t>(x.i) * P.mats[best].cols + x.j;
+    if (L.kind == DMUON_KIND_UPDATE0) x.pre_w = dbg_one(static_cast<const char*>(params[best]) + x.w_off * pb, pb, s, st);
+    smp.push_back(x);
+    return st;
+  }
+  const std::vector<int>& ch = P.chunks[L.chunk];
+  const bool sym = L.phase != kPhaseGemm;
+  for (int q = 0; q < 4; ++q) {
+    DbgSample x;
+    const int lb = rng.below(static_cast<int>(ch.size()));
+    const BucketPlan& B = P.buckets[ch[lb]];
+    x.bucket = lb;
+    x.slot = rng.below(B.count);
+    x.gm = B.mats[x.slot];
+    const int ncols = sym ? B.m : B.n;
+    x.i = rng.below(B.m);
+    x.j = (q == 2) ? std::min(x.i, ncols - 1) : rng.below(ncols);
+    x.mirror = sym && q == 3 && x.i != x.j;
+    if (L.last) {
+      const MatDev& md = P.mats[x.gm];
+      x.w_off = md.transposed ? static_cast<int64_t>(x.j) * md.cols + x.i : static_cast<int64_t>(x.i) * md.cols + x.j;
+      x.pre_w = dbg_one(static_cast<const char*>(params[x.gm]) + x.w_off * pb, pb, s, st);
+      if (st != DMUON_OK) return st;
+    }
+    smp.push_back(x);
+  }
+  return DMUON_OK;
+}
+
+dmuon_status debug_after(dmuon_plan_s& P, const Launch& L, int li, void* const* params, void* const* momenta,
+                         const std::vector<DbgSample>& smp, float lr, float mu, int nesterov, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "debug-check sync");
+  dmuon_status st = DMUON_OK;
+  const int el = P.xel, pb = dtype_bytes(P.dt.param);
+  const double f32 = std::ldexp(1.0, -22);
+  auto s_of = [&](int gm) { return dbg_one(P.ws + P.off_s + 4LL * gm, 4, s, st); };
+  if (L.kind == DMUON_KIND_MOMENTUM) {
+    for (const DbgSample& x : smp) {
+      const MatDev& md = P.mats[x.gm];
+      const double m_got = dbg_one(static_cast<const char*>(momenta[x.gm]) + x.w_off * 4, 4, s, st);
+      const int64_t u_off = md.transposed ? static_cast<int64_t>(x.j) * md.x_ld + x.i
+                                          : static_cast<int64_t>(x.i) * md.x_ld + x.j;
+      const double u_got = st == DMUON_OK ? dbg_one(P.ws + md.x0_off + u_off * el, el, s, st) : 0.0;
+      if (st != DMUON_OK) return st;
+      const double m_want = mu * x.pre_m + x.pre_g;
+      const double tm = f32 * (std::fabs(mu * x.pre_m) + std::fabs(x.pre_g)) + 1e-38;
+      if (off_by(m_got, m_want, tm)) return dbg_mismatch(P, li, L, x, "momentum", m_got, m_want, tm);
+      const double u_want = nesterov ? x.pre_g + mu * m_got : m_got;
+      const double tu = (el == 2 ? ulp_of(u_want, 2) : 0.0) + f32 * (std::fabs(x.pre_g) + std::fabs(mu * m_got)) + 1e-38;
+      if (off_by(u_got, u_want, tu)) return dbg_mismatch(P, li, L, x, "U", u_got, u_want, tu);
+    }
+    return DMUON_OK;
+  }
+  if (L.kind == DMUON_KIND_NORM) {
+    const DbgSample& x = smp[0];
+    const MatDev& md = P.mats[x.gm];
+    std::vector<double> row;
+    double ss = 0;
+    for (int r = 0; r < md.m && st == DMUON_OK; ++r) {
+      st = dbg_read(P.ws + md.x0_off + static_cast<int64_t>(r) * md.x_ld * el, md.n, el, 1, row, s);
+      for (double v : row) ss += v * v;
+    }
+    const double got = s_of(x.gm);
+    if (st != DMUON_OK) return st;
+    const double want = 1.0 / (std::sqrt(ss) + P.eps);
+    const double tol = (el == 2 ? std::ldexp(1.0, -7) : 1e-5) * want;
+    if (off_by(got, want, tol)) return dbg_mismatch(P, li, L, x, "s = 1/(|U|+eps)", got, want, tol);
+    return DMUON_OK;
+  }
+  if (L.kind == DMUON_KIND_UPDATE0) {
+    const DbgSample& x = smp[0];
+    const MatDev& md = P.mats[x.gm];
+    const int64_t u_off = md.transposed ? static_cast<int64_t>(x.j) * md.x_ld + x.i : static_cast<int64_t>(x.i) * md.x_ld + x.j;
+    const double u = dbg_one(P.ws + md.x0_off + u_off * el, el, s, st);
+    const double sn = st == DMUON_OK ? s_of(x.gm) : 0.0;
+    const double got = st == DMUON_OK ? dbg_one(static_cast<const char*>(params[x.gm]) + x.w_off * pb, pb, s, st) : 0.0;
+    if (st != DMUON_OK) return st;
+    const double want = x.pre_w - static_cast<double>(lr) * md.scale * sn * u;
+    const double tol = ulp_of(want, pb) + f32 * (std::fabs(x.pre_w) + std::fabs(lr * md.scale * sn * u)) + 1e-38;
+    if (off_by(got, want, tol)) return dbg_mismatch(P, li, L, x, "updated weight", got, want, tol);
+    return DMUON_OK;
+  }
+  const std::vector<int>& ch = P.chunks[L.chunk];
+  std::vector<double> ra, rb;
+  for (const DbgSample& x : smp) {
+    const BucketPlan& B = P.buckets[ch[x.bucket]];
+    const MatDev& md = P.mats[x.gm];
+    const View va = view_of(P, B, L.opA), vb = view_of(P, B, L.opB), vx = view_of(P, B, L.aux);
+    const int K = L.phase == kPhaseGemm ? B.m : va.inner;
+    // row i of the first operand; row j (symmetric products) or column j (gemm) of the second
+    st = dbg_read(va.base + x.slot * va.mat_bytes + static_cast<int64_t>(x.i) * va.ld * el, K, el, 1, ra, s);
+    if (st == DMUON_OK) {
+      if (L.phase == kPhaseGemm)
+        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(x.j) * el, K, el, vb.ld, rb, s);
+      else
+        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(x.j) * vb.ld * el, K, el, 1, rb, s);
+    }
+    if (st != DMUON_OK) return st;
+    double acc = 0, mag = 0;
+    for (int k = 0; k < K; ++k) {
+      acc += ra[k] * rb[k];
+      mag += std::fabs(ra[k] * rb[k]);
+    }
+    const double sn = L.first ? s_of(x.gm) : 1.0;
+    if (st != DMUON_OK) return st;
+    double want, tol;
+    const double acc_err = std::ldexp(1.0, -20) * mag;  // fp32 accumulation over K, generously
+    if (L.kind == DMUON_KIND_POLY) {
+      const double a = dbg_one(vx.base + x.slot * vx.mat_bytes + (static_cast<int64_t>(x.i) * vx.ld + x.j) * el, el, s, st);
+      want = L.b * a + L.c * acc + (x.i == x.j ? L.diag : 0.0);
+      tol = std::fabs(L.c) * acc_err + f32 * (std::fabs(L.b * a) + std::fabs(L.c * acc) + std::fabs(L.diag));
+    } else if (L.phase != kPhaseGemm) {  // X X^T (scaled by s^2 at step 0) or a product of two symmetric matrices
+      want = (L.kind == DMUON_KIND_GRAM && L.first ? sn * sn : 1.0) * acc;
+      tol = (L.kind == DMUON_KIND_GRAM && L.first ? sn * sn : 1.0) * acc_err;
+    } else {
+      double ax = 0;
+      if (L.a != 0.f)
+        ax = dbg_one(vx.base + x.slot * vx.mat_bytes + (static_cast<int64_t>(x.i) * vx.ld + x.j) * el, el, s, st);
+      want = sn * (acc + L.a * ax);
+      tol = sn * (acc_err + f32 * (std::fabs(acc) + std::fabs(L.a * ax)));
+    }
+    if (st != DMUON_OK) return st;
+    if (!L.last) {
+      const View vo = view_of(P, B, L.out);
+      const char* po = vo.base + x.slot * vo.mat_bytes;
+      const double got = dbg_one(po + (static_cast<int64_t>(x.i) * vo.ld + x.j) * el, el, s, st);
+      if (st != DMUON_OK) return st;
+      const double t = tol + ulp_of(want, el) + 1e-38;
+      if (off_by(got, want, t)) return dbg_mismatch(P, li, L, x, "product", got, want, t);
+      if (x.mirror) {  // the mirrored element holds the same stored value, bit for bit
+        const double mir = dbg_one(po + (static_cast<int64_t>(x.j) * vo.ld + x.i) * el, el, s, st);
+        if (st != DMUON_OK) return st;
+        if (!(mir == got)) return dbg_mismatch(P, li, L, x, "mirror (j, i) of the product", mir, got, 0.0);
+      }
+    } else {  // the weight update of the last product
+      const double step = static_cast<double>(lr) * md.scale;
+      const double got = dbg_one(static_cast<const char*>(params[x.gm]) + x.w_off * pb, pb, s, st);
+      if (st != DMUON_OK) return st;
+      const double wwant = x.pre_w - step * want;
+      const double t = ulp_of(wwant, pb) + step * tol + f32 * (std::fabs(x.pre_w) + std::fabs(step * want)) + 1e-38;
+      if (off_by(got, wwant, t)) return dbg_mismatch(P, li, L, x, "updated weight", got, wwant, t);
+    }
+  }
+  return DMUON_OK;
 }
 
 }  // namespace
@@ -816,7 +1153,7 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES |
-                DMUON_FLAG_EPILOGUE_AX | DMUON_FLAG_STATIC_TILES))
+                DMUON_FLAG_EPILOGUE_AX | DMUON_FLAG_STATIC_TILES | DMUON_FLAG_DEBUG_CHECKS))
     return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
@@ -1164,9 +1501,18 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     if (static_cast<int>(li) == P->first_w_launch && P->w_wait != nullptr &&
         (e = cudaStreamWaitEvent(s, P->w_wait, 0)) != cudaSuccess)
       return cuda_fail(e, "cudaStreamWaitEvent (weight events)");
+    std::vector<DbgSample> dbg;
+    const bool debug = (P->flags & DMUON_FLAG_DEBUG_CHECKS) != 0;
+    if (debug) {
+      dmuon_status sd = debug_before(*P, L, static_cast<int>(li), params, grads, momenta, dbg, s);
+      if (sd != DMUON_OK) return sd;
+    }
     dmuon_status st = record_launch(*P, L, s, true);
     if (st != DMUON_OK) return st;
-    if (L.kind == DMUON_KIND_MOMENTUM) {
+    if (debug && test_skip_launch(static_cast<int>(li))) {
+      // test hook (debug mode only): the launch is left out, so its outputs keep what was there
+      e = cudaSuccess;
+    } else if (L.kind == DMUON_KIND_MOMENTUM) {
       e = launch_momentum(sp, L.grid, s);
     } else if (L.kind == DMUON_KIND_NORM) {
       e = launch_norm_finalize(sp, L.grid, s);
@@ -1191,6 +1537,10 @@ dmuon_status dmuon_step(dmuon_plan_t P, void* const* params, const void* const* 
     ++P->launch_count;
     st = record_launch(*P, L, s, false);
     if (st != DMUON_OK) return st;
+    if (debug) {
+      st = debug_after(*P, L, static_cast<int>(li), params, momenta, dbg, lr, mu, nesterov, s);
+      if (st != DMUON_OK) return st;
+    }
     if (static_cast<int>(li) == P->last_w_launch && P->w_done != nullptr &&
         (e = cudaEventRecord(P->w_done, s)) != cudaSuccess)
       return cuda_fail(e, "cudaEventRecord (weight events)");
@@ -1239,9 +1589,10 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
   char t[512];
   snprintf(t, sizeof t,
            "\"n_mats\": %zu, \"ns_steps\": %d, \"compute\": \"%s\", \"tile\": [%d, %d], \"workspace_bytes\": %zu, "
-           "\"stream_units\": %lld, \"chunks\": %zu, ",
+           "\"stream_units\": %lld, \"chunks\": %zu, \"tuned\": %s, \"tune_timed_buckets\": %d, "
+           "\"tune_cached_buckets\": %d, ",
            P->mats.size(), P->ns_steps, P->tc ? "bf16" : "f32", P->tile_m, P->tile_n, P->ws_bytes,
-           (long long)P->n_units, P->chunks.size());
+           (long long)P->n_units, P->chunks.size(), P->tuned ? "true" : "false", P->tune_timed, P->tune_cached);
   j += t;
   j += "\"buckets\": [";
   for (size_t b = 0; b < P->buckets.size(); ++b) {

@@ -36,6 +36,7 @@ FLAG_TUNE = 0x4
 FLAG_PAIR_TILES = 0x8
 FLAG_EPILOGUE_AX = 0x10
 FLAG_STATIC_TILES = 0x20
+FLAG_DEBUG_CHECKS = 0x40
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 

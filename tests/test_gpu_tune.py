@@ -23,8 +23,10 @@ def test_tuned_plan_matches_oracle_and_reports_costs(gram):
     muon = dm.Muon.create(SHAPES, flags=dm.FLAG_CAPTURE_UPDATE | dm.FLAG_TUNE | (dm.FLAG_GRAM_NS if gram else 0))
     run.muon = muon
     d = muon.plan.describe()
+    assert d["tuned"] and d["tune_timed_buckets"] + d["tune_cached_buckets"] == len(d["buckets"])
     for b in d["buckets"]:
         assert b["bn_sym"] in (128, 256) and b["bn_gemm"] in (128, 256), b
+        assert not b["pair"] or b["bn_sym"] == b["bn_gemm"] == 256, b
         assert all(t > 0 for t in b["tile_ms"]), b
     init = _fill(run, 3100)
     run.step()
@@ -40,3 +42,14 @@ def test_tuned_plan_matches_oracle_and_reports_costs(gram):
     own, load = dm.dmuon_assign_owners(SHAPES, 4, costs=costs)
     assert sorted(set(own)) == [0, 1, 2, 3]
     np.testing.assert_allclose(sum(load), sum(costs), rtol=1e-12)
+
+
+def test_second_tuned_plan_reuses_the_cached_timings():
+    shapes = [(1536, 8960), (8960, 1536), (1536, 1536), (256, 1536)]
+    first = dm.Muon.create(shapes, flags=dm.FLAG_TUNE)
+    second = dm.Muon.create(shapes, flags=dm.FLAG_TUNE)
+    a, b = first.plan.describe(), second.plan.describe()
+    assert b["tuned"] and b["tune_timed_buckets"] == 0 and b["tune_cached_buckets"] == len(b["buckets"])
+    # the same choices and per-tile costs as the plan that timed them
+    key = ("m", "n", "pair", "bn_sym", "bn_gemm", "tile_ms")
+    assert [{k: x[k] for k in key} for x in a["buckets"]] == [{k: x[k] for k in key} for x in b["buckets"]]
