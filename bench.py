@@ -474,7 +474,8 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
 def plan_flags(args):
     from matrix_optimizer_update_gb300 import dmuon as dm
 
-    return (dm.FLAG_PAIR_TILES if args.pair else 0) | (dm.FLAG_STATIC_TILES if args.static_tiles else 0)
+    return ((dm.FLAG_PAIR_TILES if args.pair else 0) | (dm.FLAG_STATIC_TILES if args.static_tiles else 0)
+            | (dm.FLAG_TUNE if args.tune else 0))
 
 
 def run_ours(args):
@@ -620,6 +621,8 @@ def run_ours(args):
         plan.set_weight_events(w_copied.cuda_event, w_ready.cuda_event)
         torch.cuda.synchronize()
         barrier()
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(e2e_steps)]
         t0 = time.perf_counter()
         bits = 0
         with torch.cuda.stream(copy_stream):
@@ -635,7 +638,9 @@ def run_ours(args):
                     gbuf[nb].copy_(hG, non_blocking=True)
                     copied[nb].record(copy_stream)
             stream.wait_event(copied[b])
+            step_ev[k][0].record(stream)
             plan.step(Wp, gptrs[b], Mp, w.lr, w.mu, w.nesterov, sh)  # W writes wait for w_copied
+            step_ev[k][1].record(stream)
             used[b].record(stream)
             with torch.cuda.stream(d2h_stream):  # this step's weights back to the host
                 d2h_stream.wait_event(w_ready)
@@ -645,11 +650,13 @@ def run_ours(args):
         torch.cuda.synchronize()
         wall_ms = (time.perf_counter() - t0) * 1e3
         plan.set_weight_events(0, 0)
+        dev_ms = sum(a.elapsed_time(b) for a, b in step_ev) / e2e_steps
         returned_ok = bool(torch.equal(hW.to(ms.W.device), ms.W))
         barrier()
         e2e_ms = max_over_ranks(wall_ms, world, f"cuda:{local}")
         e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
+               "device_ms_per_step": dev_ms,
                "h2d_bytes_per_step": hG.numel() * hG.element_size(),
                "d2h_bytes_per_step": hW.numel() * hW.element_size() + 4,
                "result_read": "every updated weight (to host memory) and the device status word, every step",
@@ -727,6 +734,7 @@ def run_ours(args):
                    "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
                    "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
                    "tile_schedule": "dealt round-robin" if args.static_tiles else "claimed from a counter",
+                   "tuned": bool(args.tune),
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
         "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
@@ -763,6 +771,7 @@ def main(argv=None):
     ap.add_argument("--per-workload-steps", type=int, default=5, help="timed steps per other matrix set")
     ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
     ap.add_argument("--static-tiles", action="store_true", help="deal tiles round-robin instead of claiming them")
+    ap.add_argument("--tune", action="store_true", help="choose tile configurations by timing them at bind")
     ap.add_argument("--adamw", action="store_true",
                     help="also time the AdamW kernel over Llama-3.1-8B's non-matrix parameters")
     args = ap.parse_args(argv)

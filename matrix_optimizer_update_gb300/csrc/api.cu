@@ -327,8 +327,8 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn_gemm(order[b].second) : kSimtBN;
-    // two-SM 256 x 256 tiles where both dimensions fill them
-    P.buckets[b].pair = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES) && order[b].first >= 256 &&
+    // two-SM 256 x 256 tiles where both dimensions fill them: no 256-row tile is left half empty
+    P.buckets[b].pair = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES) && order[b].first % 256 == 0 &&
                         P.buckets[b].bn_sym == 256 && P.buckets[b].bn_gemm == 256;
   }
 
