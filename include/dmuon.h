@@ -96,7 +96,11 @@ typedef struct {
                                           of 256 and whose products run 256 wide use
                                           256 x 256 tiles on pairs of SMs
                                           (two-SM UMMA, thread-block clusters of
-                                          2). bf16 only.                        */
+                                          2). bf16 only. Test hook: with the
+                                          environment variable
+                                          DMUON_TEST_FORCE_PAIRS=1, every bucket
+                                          with a short side >= 256 gets pairs (as
+                                          DMUON_FLAG_TUNE may choose).           */
 #define DMUON_FLAG_EPILOGUE_AX 0x10u   /* standard form: add the a*X_k term of the
                                           quintic step in the epilogue of the
                                           product B X_k (reading the X_k tile),

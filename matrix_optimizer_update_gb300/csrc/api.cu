@@ -103,6 +103,14 @@ bool test_hook(const char* where) {
   return v != nullptr && std::strcmp(v, where) == 0;
 }
 
+// Test hook: true when the environment variable `name` is set to a non-empty value other than "0".
+// DMUON_TEST_FORCE_PAIRS with DMUON_FLAG_PAIR_TILES gives every bucket with a short side >= 256
+// two-SM pair tiles (as tuning may), also where the short side is not a multiple of 256.
+bool test_hook_env(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
 // Test hook of the debug checks: DMUON_TEST_SKIP_LAUNCH=<i> leaves launch i of
 // every step out (only under DMUON_FLAG_DEBUG_CHECKS), so that its outputs are
 // stale and the checks must report them.
@@ -328,8 +336,12 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn_gemm(order[b].second) : kSimtBN;
     // two-SM 256 x 256 tiles where both dimensions fill them: no 256-row tile is left half empty
-    P.buckets[b].pair = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES) && order[b].first % 256 == 0 &&
-                        P.buckets[b].bn_sym == 256 && P.buckets[b].bn_gemm == 256;
+    // (tuning may still choose them for other short sides >= 256, and so does the test hook)
+    const bool pair_flag = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES);
+    const bool forced = pair_flag && order[b].first >= 256 && test_hook_env("DMUON_TEST_FORCE_PAIRS");
+    if (forced) P.buckets[b].bn_sym = P.buckets[b].bn_gemm = 256;
+    P.buckets[b].pair = forced || (pair_flag && order[b].first % 256 == 0 && P.buckets[b].bn_sym == 256 &&
+                                   P.buckets[b].bn_gemm == 256);
   }
 
   P.mats.assign(n_mats, MatDev{});
@@ -466,8 +478,10 @@ dmuon_status finish_plan(dmuon_plan_s& P) {
   P.off_probe = take((int64_t)sizeof(int4) * kProbeTiles);
   // per launch of a step (and one for the tuning probes): the tile-claim counter pair, 128 bytes
   // apart; and the per-CTA profiling records of each launch. The launch count is bounded by the
-  // step's sequence below: 3 + (4 * ns_steps) per chunk at most.
-  const int64_t max_launches = 3 + 4LL * std::max(P.ns_steps, 1) * std::max<int64_t>((int64_t)P.chunks.size(), 1);
+  // step's sequence below, 3 + 4 * ns_steps per launch chunk at most, and a chunk holds at least one
+  // bucket. The bound uses the bucket count, which tuning does not change (it may split buckets
+  // into more chunks): the layout of the workspace must not move when tuning re-plans.
+  const int64_t max_launches = 3 + 4LL * std::max(P.ns_steps, 1) * std::max<int64_t>((int64_t)P.buckets.size(), 1);
   P.off_sched = take(kSchedBytes * (max_launches + 1));
   P.off_probe_sched = P.off_sched + kSchedBytes * max_launches;
   P.off_cta = take(16LL * kMaxCtaRecords * max_launches);
@@ -803,21 +817,29 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         auto launch = [&]() {
           return T.pair ? launch_tc_pair(phase, tp, grid, s) : launch_tc(phase, T.bn_sym, tp, grid, s);
         };
+        // Timed long enough for the clock to settle under the power limit: about 30 ms untimed,
+        // then about 60 ms timed. A configuration that does more work per clock but draws more
+        // power is then measured at the clock it gets in a long step, not at an idle GPU's clock.
+        auto run = [&](int reps, float* ms) -> cudaError_t {
+          cudaError_t r = cudaEventRecord(e0, s);
+          for (int rep = 0; rep < reps && r == cudaSuccess; ++rep) r = launch();
+          if (r == cudaSuccess) r = cudaEventRecord(e1, s);
+          if (r == cudaSuccess) r = cudaEventSynchronize(e1);
+          if (r == cudaSuccess) r = cudaEventElapsedTime(ms, e0, e1);
+          return r;
+        };
         float ms = 0.f;
-        if ((e = launch()) != cudaSuccess || (e = cudaEventRecord(e0, s)) != cudaSuccess) {
-          st = cuda_fail(e, "tuning launch");
-          break;
-        }
-        for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) e = launch();
-        if (e == cudaSuccess) e = cudaEventRecord(e1, s);
-        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
-        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+        e = run(1, &ms);  // also the first launch of this kernel
+        const double per = std::max(ms, 0.01f);
+        if (e == cudaSuccess) e = run(static_cast<int>(std::min(400.0, std::ceil(30.0 / per))), &ms);
+        const int reps = static_cast<int>(std::min(400.0, std::max(3.0, std::ceil(60.0 / per))));
+        if (e == cudaSuccess) e = run(reps, &ms);
         if (e != cudaSuccess) {
           st = cuda_fail(e, "tuning run");
           break;
         }
         const int waves = (n + grid - 1) / grid;
-        tt.sm_ms[ci][kind] = ms / 3.0 / waves * (T.pair ? 2.0 : 1.0);  // SMs a tile occupies
+        tt.sm_ms[ci][kind] = ms / reps / waves * (T.pair ? 2.0 : 1.0);  // SMs a tile occupies
       }
     }
     if (st != DMUON_OK) break;
@@ -865,7 +887,16 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
   cudaEventDestroy(e1);
   if (st != DMUON_OK) return st;
   P.tuned = true;
-  return finish_plan(P);
+  // re-plan with the chosen configurations; the workspace layout the caller sized must not move
+  std::vector<int64_t> before;
+  for (const BucketPlan& B : P.buckets) before.insert(before.end(), std::begin(B.off), std::end(B.off));
+  before.insert(before.end(), {P.off_items, P.off_sched, P.off_cta, P.off_capture, (int64_t)P.ws_bytes});
+  if ((st = finish_plan(P)) != DMUON_OK) return st;
+  std::vector<int64_t> after;
+  for (const BucketPlan& B : P.buckets) after.insert(after.end(), std::begin(B.off), std::end(B.off));
+  after.insert(after.end(), {P.off_items, P.off_sched, P.off_cta, P.off_capture, (int64_t)P.ws_bytes});
+  if (after != before) return fail(DMUON_ERR_WORKSPACE, "internal: tuning moved the workspace layout");
+  return DMUON_OK;
 }
 
 // ------------------------------------------------------------------ debug checks
@@ -1072,13 +1103,18 @@ dmuon_status debug_after(dmuon_plan_s& P, const Launch& L, int li, void* const* 
     const MatDev& md = P.mats[x.gm];
     const View va = view_of(P, B, L.opA), vb = view_of(P, B, L.opB), vx = view_of(P, B, L.aux);
     const int K = L.phase == kPhaseGemm ? B.m : va.inner;
-    // row i of the first operand; row j (symmetric products) or column j (gemm) of the second
-    st = dbg_read(va.base + x.slot * va.mat_bytes + static_cast<int64_t>(x.i) * va.ld * el, K, el, 1, ra, s);
+    // row i of the first operand; row j (symmetric products) or column j (gemm) of the second. A
+    // symmetric product is computed on the upper element (r, c), r <= c, and mirrored, so the
+    // element at (i, j) is the one computed from rows min(i, j) and max(i, j): with two different
+    // operands (the Gram-space form) the two orders differ by the operands' rounding.
+    const bool sym = L.phase != kPhaseGemm;
+    const int r = sym ? std::min(x.i, x.j) : x.i, c = sym ? std::max(x.i, x.j) : x.j;
+    st = dbg_read(va.base + x.slot * va.mat_bytes + static_cast<int64_t>(r) * va.ld * el, K, el, 1, ra, s);
     if (st == DMUON_OK) {
       if (L.phase == kPhaseGemm)
-        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(x.j) * el, K, el, vb.ld, rb, s);
+        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(c) * el, K, el, vb.ld, rb, s);
       else
-        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(x.j) * vb.ld * el, K, el, 1, rb, s);
+        st = dbg_read(vb.base + x.slot * vb.mat_bytes + static_cast<int64_t>(c) * vb.ld * el, K, el, 1, rb, s);
     }
     if (st != DMUON_OK) return st;
     double acc = 0, mag = 0;
@@ -1293,6 +1329,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   if ((P->flags & DMUON_FLAG_TUNE) && P->tc && P->ns_steps > 0) {
     dmuon_status st = tune_plan(*P, s);
     if (st != DMUON_OK) return st;
+    if (P->ws_bytes > bytes) return fail(DMUON_ERR_WORKSPACE, "internal: the tuned plan needs more workspace");
     if ((e = up(P->off_items, P->items.data(), sizeof(int4) * P->items.size())) != cudaSuccess ||
         (e = cudaMemsetAsync(ws + P->off_status, 0, 4, s)) != cudaSuccess || (e = cudaStreamSynchronize(s)) != cudaSuccess)
       return cuda_fail(e, "tuned table upload");

@@ -100,3 +100,27 @@ def test_pair_and_one_sm_tiles_agree_bitwise(gram):
     b.step()
     torch.cuda.synchronize()
     assert torch.equal(a.W, b.W) and torch.equal(a.M, b.M)
+
+
+RAGGED_PAIRS = [(300, 700), (700, 300), (520, 1000), (1408, 2048), (2048, 1408), (640, 640), (384, 384)]
+
+
+@pytest.mark.parametrize("gram", [False, True])
+def test_pair_tiles_on_short_sides_not_a_multiple_of_256(gram, monkeypatch):
+    """Pairs on short sides that leave the last row pair half empty (the second CTA's rows all past the
+    matrix): what tuning may choose. Oracle parity, and the same bits as one-SM tiles."""
+    monkeypatch.setenv("DMUON_TEST_FORCE_PAIRS", "1")
+    run = LibRun(RAGGED_PAIRS, pair=True, gram_ns=gram)
+    monkeypatch.delenv("DMUON_TEST_FORCE_PAIRS")
+    assert all(b["pair"] for b in run.muon.plan.describe()["buckets"])
+    one = LibRun(RAGGED_PAIRS, pair=False, gram_ns=gram)
+    init = _fill(run, 5700, m_std=1e-3)
+    one.W.copy_(run.W)
+    one.G.copy_(run.G)
+    one.M.copy_(run.M)
+    run.step()
+    one.step()
+    torch.cuda.synchronize()
+    assert run.status() == 0 and one.status() == 0
+    _check_all(run, init)
+    assert torch.equal(run.W, one.W) and torch.equal(run.M, one.M)
