@@ -621,12 +621,17 @@ def run_ours(args):
         plan.set_weight_events(w_copied.cuda_event, w_ready.cuda_event)
         torch.cuda.synchronize()
         barrier()
-        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(e2e_steps)]
+        def ev_pairs():
+            return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(e2e_steps)]
+
+        step_ev, h2d_ev, d2h_ev = ev_pairs(), ev_pairs(), ev_pairs()
         t0 = time.perf_counter()
         bits = 0
         with torch.cuda.stream(copy_stream):
+            h2d_ev[0][0].record(copy_stream)
             gbuf[0].copy_(hG, non_blocking=True)
+            h2d_ev[0][1].record(copy_stream)
             copied[0].record(copy_stream)
         for k in range(e2e_steps):
             b = k & 1
@@ -635,7 +640,9 @@ def run_ours(args):
                 with torch.cuda.stream(copy_stream):
                     if k >= 1:
                         copy_stream.wait_event(used[nb])
+                    h2d_ev[k + 1][0].record(copy_stream)
                     gbuf[nb].copy_(hG, non_blocking=True)
+                    h2d_ev[k + 1][1].record(copy_stream)
                     copied[nb].record(copy_stream)
             stream.wait_event(copied[b])
             step_ev[k][0].record(stream)
@@ -644,19 +651,24 @@ def run_ours(args):
             used[b].record(stream)
             with torch.cuda.stream(d2h_stream):  # this step's weights back to the host
                 d2h_stream.wait_event(w_ready)
+                d2h_ev[k][0].record(d2h_stream)
                 hW.copy_(ms.W, non_blocking=True)
+                d2h_ev[k][1].record(d2h_stream)
                 w_copied.record(d2h_stream)
             bits |= plan.read_device_status(sh)
         torch.cuda.synchronize()
         wall_ms = (time.perf_counter() - t0) * 1e3
         plan.set_weight_events(0, 0)
         dev_ms = sum(a.elapsed_time(b) for a, b in step_ev) / e2e_steps
+        h2d_gbs = hG.numel() * hG.element_size() * e2e_steps / (sum(a.elapsed_time(b) for a, b in h2d_ev) * 1e-3) / 1e9
+        d2h_gbs = hW.numel() * hW.element_size() * e2e_steps / (sum(a.elapsed_time(b) for a, b in d2h_ev) * 1e-3) / 1e9
         returned_ok = bool(torch.equal(hW.to(ms.W.device), ms.W))
         barrier()
         e2e_ms = max_over_ranks(wall_ms, world, f"cuda:{local}")
         e2e = {"value": aggregate(tot["ns_flops"], e2e_steps, world, e2e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
                "device_ms_per_step": dev_ms,
+               "copy_gbs_in_loop": {"h2d": h2d_gbs, "d2h": d2h_gbs},
                "h2d_bytes_per_step": hG.numel() * hG.element_size(),
                "d2h_bytes_per_step": hW.numel() * hW.element_size() + 4,
                "result_read": "every updated weight (to host memory) and the device status word, every step",

@@ -90,6 +90,7 @@ dmuon_status cuda_fail(cudaError_t e, const char* what) {
 constexpr int64_t kAlign = 1024;
 constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
 constexpr int64_t kSchedBytes = 128;   // one launch's tile-claim counters (own cache line)
+constexpr int64_t kPrefetchMaxBytes = 16LL << 20;  // largest operand set per matrix prefetched into L2
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -134,6 +135,7 @@ struct BucketPlan {
   // measured SM-ms per tile (time per tile x SMs it occupies): X X^T (K = n), m x m products, gemm;
   // 0 = not measured
   double tile_ms[3] = {0, 0, 0};
+  double tune_cost[3] = {0, 0, 0};  // tuning: SM-ms per matrix of one-SM 128, one-SM 256, pairs (0 = not timed)
   std::vector<int32_t> mats;  // slot -> global matrix index
   int64_t off_slotmat = -1;
   int64_t off[kBufCount] = {-1, -1, -1, -1, -1, -1, -1};
@@ -684,6 +686,20 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
     st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != DMUON_OK) return st;
   }
+  // operands worth prefetching into L2 a wave ahead: a matrix's operands must be small next to
+  // the L2 (so that a wave of them plus the next fit), and every operand matrix is contiguous
+  // (one bucket slot) with a 16-byte multiple size
+  const int64_t op_bytes = va.mat_bytes + (opB != opA ? vb.mat_bytes : 0);
+  if (op_bytes <= kPrefetchMaxBytes) {
+    tb.pf_base[0] = va.base;
+    tb.pf_stride[0] = va.mat_bytes;
+    tb.pf_bytes[0] = va.mat_bytes / 16 * 16;
+    if (opB != opA) {
+      tb.pf_base[1] = vb.base;
+      tb.pf_stride[1] = vb.mat_bytes;
+      tb.pf_bytes[1] = vb.mat_bytes / 16 * 16;
+    }
+  }
   tb.out = vo.base;
   tb.out_mat_stride = vo.mat_bytes;
   tb.out_ld = vo.ld;
@@ -772,6 +788,16 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         cached = true;
       }
     }
+    if (!cached) {
+      // realistic operands for the probes: X0 and A of the first slots the probes touch
+      const int slots = std::min(B.count, 8);
+      if ((e = launch_tuning_fill(P.ws + B.off[kBufX0], B.x_mat_bytes * slots, 17u, 4 * P.num_sms, s)) !=
+              cudaSuccess ||
+          (e = launch_tuning_fill(P.ws + B.off[kBufA], B.a_mat_bytes * slots, 29u, 4 * P.num_sms, s)) != cudaSuccess) {
+        st = cuda_fail(e, "tuning fill");
+        break;
+      }
+    }
     for (int ci = 0; ci < kTuneCands && st == DMUON_OK && !cached; ++ci) {
       BucketPlan T = B;
       T.bn_sym = T.bn_gemm = kTuneCandBn[ci];
@@ -792,9 +818,9 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
           phase = kPhaseGram, opA = opB = kBufX0, out = kBufA;
         } else if (kind == 1) {
           phase = kPhaseGram, opA = opB = kBufA, out = B.off[kBufB] >= 0 ? kBufB : kBufQ0;
-        } else {
-          // writes over its own operand: the values are garbage, only the time is used
-          phase = kPhaseGemm, opA = kBufA, opB = kBufX0, out = kBufX0, aux = kBufX0;
+        } else {  // the output goes to a buffer that no probe reads (values unused, only the time)
+          const int spare = B.off[kBufX1] >= 0 ? kBufX1 : (B.off[kBufR] >= 0 ? kBufR : kBufX0);
+          phase = kPhaseGemm, opA = kBufA, opB = kBufX0, out = spare, aux = kBufX0;
         }
         TcParams tp;
         std::memset(&tp, 0, sizeof(tp));
@@ -869,6 +895,7 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
       add_tiles(P, DMUON_KIND_GEMM, 0, T, tiles);
       cg[ci] = tiles.size() * n_gm * tt.sm_ms[ci][2];
     }
+    for (int ci = 0; ci < kTuneCands; ++ci) B.tune_cost[ci] = cs[ci] + cg[ci] < 1e299 ? cs[ci] + cg[ci] : 0.0;
     const int bs = cs[0] <= cs[1] ? 0 : 1, bg = cg[0] <= cg[1] ? 0 : 1;  // best one-SM widths
     if (cs[2] + cg[2] < cs[bs] + cg[bg]) {
       B.pair = true;
@@ -1637,9 +1664,10 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
     snprintf(t, sizeof t,
              "%s{\"m\": %d, \"n\": %d, \"count\": %d, \"transposed\": %d, \"x_ld\": %d, \"m_ld\": %d, "
              "\"form\": \"%s\", \"pair\": %s, \"bn_sym\": %d, \"bn_gemm\": %d, "
-             "\"tile_ms\": [%.6g, %.6g, %.6g]}",
+             "\"tile_ms\": [%.6g, %.6g, %.6g], \"tune_cost\": [%.6g, %.6g, %.6g]}",
              b ? ", " : "", B.m, B.n, B.count, B.n_transposed, B.x_ld, B.m_ld, B.gram ? "gram" : "standard",
-             B.pair ? "true" : "false", B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2]);
+             B.pair ? "true" : "false", B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2],
+             B.tune_cost[0], B.tune_cost[1], B.tune_cost[2]);
     j += t;
   }
   j += "], \"regions\": {";

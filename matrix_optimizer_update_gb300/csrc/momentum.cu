@@ -335,4 +335,36 @@ cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ tuning data
+// Fills n bf16 elements (n a multiple of 8, dst 16-byte aligned) with values in [-1/64, 1/64) from a
+// counter-based hash of the element index: operands for bind-time tuning probes, so that the tensor
+// cores are timed on data whose bits toggle like real operands (on zeros they draw less power and
+// run at a clock the real step does not get). Not part of the update's arithmetic.
+__global__ void __launch_bounds__(kStreamThreads) tuning_fill_kernel(uint4* dst, int64_t n8, uint32_t seed) {
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n8; v += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x = static_cast<uint32_t>(v) * 4u + q + seed * 0x9E3779B9u;
+      x ^= x >> 16;
+      x *= 0x7FEB352Du;
+      x ^= x >> 15;
+      x *= 0x846CA68Bu;
+      x ^= x >> 16;
+      // two bf16 values from the hash's halves: sign, exponent 2^-7..2^-14, 7 mantissa bits
+      const uint32_t lo = (x & 0x807Fu) | ((0x78u - ((x >> 8) & 7u)) << 7);
+      const uint32_t hi = ((x >> 16) & 0x807Fu) | ((0x78u - ((x >> 24) & 7u)) << 7);
+      h[q] = lo | (hi << 16);
+    }
+    dst[v] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+cudaError_t launch_tuning_fill(void* dst, int64_t bytes, uint32_t seed, int grid, cudaStream_t s) {
+  const int64_t n8 = bytes / 16;
+  if (n8 <= 0) return cudaSuccess;
+  tuning_fill_kernel<<<grid, kStreamThreads, 0, s>>>(reinterpret_cast<uint4*>(dst), n8, seed);
+  return cudaGetLastError();
+}
+
 }  // namespace dmuon

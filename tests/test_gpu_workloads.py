@@ -76,7 +76,10 @@ def test_workload_parity(name, gram, pair, ax):
         nrm = float(torch.linalg.vector_norm(x[: r * c])) / np.sqrt(min(r, c))
         assert 0.68 <= nrm <= 1.21, (i, r, c, nrm)
 
-    worst = {"x": 0.0, "w": 0.0, "m": 0.0}
+    # The default form keeps its stored weights at least 5 % under the 1e-3 bar on every workload
+    # (measured worst: MoE 9.1e-4); the opt-in forms are held to the bar itself.
+    w_bar = TOL_W[w.param_dtype] * (0.95 if not (gram or pair or ax) else 1.0)
+    worst = {"x": 0.0, "w": 0.0, "m": 0.0, "worst_w_matrix": None}
     for i in idx:
         r, c = w.shapes[i]
         W0, G, M0 = before[i]
@@ -89,9 +92,11 @@ def test_workload_parity(name, gram, pair, ax):
         ex = rel(Xg, Xr)
         ew = float(np.linalg.norm(Wg - ref.round_to_dtype(Wr, w.param_dtype)) / np.linalg.norm(Wr))
         em = rel(Mg, Mr)
-        worst = {"x": max(worst["x"], ex), "w": max(worst["w"], ew), "m": max(worst["m"], em)}
+        if ew > worst["w"]:
+            worst["worst_w_matrix"] = (i, r, c)
+        worst.update(x=max(worst["x"], ex), w=max(worst["w"], ew), m=max(worst["m"], em))
         assert ex <= TOL_X[w.compute], (i, r, c, ex)
-        assert ew <= TOL_W[w.param_dtype], (i, r, c, ew)
+        assert ew <= w_bar, (i, r, c, ew, w_bar)
         assert em <= TOL_M, (i, r, c, em)
         assert weight_rounding_violations(Wg, Wr, W0, Xg, Xr, w.lr * ref.update_scale(r, c), w.param_dtype) == 0
     print(name, "gram" if gram else "standard", "pair" if pair else "", "aX-epilogue" if ax else "", "sampled",
