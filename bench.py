@@ -366,6 +366,13 @@ def timed_steps(plan, step, steps, stream, launches_per_step, local, world, barr
     prof = plan.profile_end(steps * launches_per_step)
     clk = clocks.stop() if clocks else None
     status = plan.read_device_status(stream.cuda_stream)
+    # the first timed step, launch by launch: ms of each product per Newton-Schulz step
+    by_step = {}
+    for (kind, kms, _), L in zip(prof[:launches_per_step], plan.describe()["launches"]):
+        if L["step"] >= 0:
+            by_step.setdefault(dm.KIND_NAMES[kind], {}).setdefault(L["step"], 0.0)
+            by_step[dm.KIND_NAMES[kind]][L["step"]] += kms
+    timed_steps.last_by_step = {k: [round(v[t], 4) for t in sorted(v)] for k, v in by_step.items()}
     per_kind = {}
     for kind, kms, work in prof:
         d = per_kind.setdefault(dm.KIND_NAMES[kind], {"ms": 0.0, "work": 0.0, "launches": 0})
@@ -463,12 +470,20 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
                (ns_tflops / peak) if ns_tflops else None,
            "compute": w.compute, "kernels": kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, w.compute,
                                                          w.name),
+           "ms_by_ns_step": timed_steps.last_by_step,
+           **({"tuned_buckets": tuned_buckets(plan)} if args.tune else {}),
            "gpu_launches": launches, "device_status": status, "clocks": clk,
            "cta_tails": cta_tails(plan, step, stream) if w.compute == "bf16" else None}
     del muon, plan, ms
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
+
+
+def tuned_buckets(plan):
+    """A tuned plan's choice per bucket, with the measured cost (SM-ms per matrix) of each candidate:
+    one-SM 128 wide, one-SM 256 wide, two-SM pairs (0 = not timed)."""
+    return [{k: b[k] for k in ("m", "n", "pair", "bn_sym", "bn_gemm", "tune_cost")} for b in plan.describe()["buckets"]]
 
 
 def plan_flags(args):
@@ -511,6 +526,7 @@ def run_ours(args):
     plan = muon.plan
     desc = plan.describe()
     launches_per_step = len(desc["launches"])
+    headline_buckets = tuned_buckets(plan) if args.tune else None
     Wp, Gp, Mp = ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M)
     sh = stream.cuda_stream
 
@@ -532,6 +548,7 @@ def run_ours(args):
     # ---- device-resident timed region
     max_ms, per_kind, launches, status, clk = timed_steps(plan, step, args.steps, stream, launches_per_step, local,
                                                           world, barrier)
+    ms_by_ns_step = timed_steps.last_by_step
 
     # ---- per-kind accounting from the live events
     ns_ms = sum(per_kind.get(k, {}).get("ms", 0.0) for k in NS_KINDS) / args.steps
@@ -747,11 +764,12 @@ def run_ours(args):
                    "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
                    "tile_schedule": "dealt round-robin" if args.static_tiles else "claimed from a counter",
                    "tuned": bool(args.tune),
+                   **({"tuned_buckets": headline_buckets} if args.tune else {}),
                    "l2": "inputs larger than L2 (whole matrix set resident in HBM, no flush needed)"},
         "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
         "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
         "ns_frac_of_sustained_peak": ns_tflops / tensor_peak if ns_tflops else None,
-        "kernels": kernels, "cta_tails": tails, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
+        "kernels": kernels, "ms_by_ns_step": ms_by_ns_step, "cta_tails": tails, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
         "per_workload": per_workload,
         **({"adamw_other_params": adamw} if adamw is not None else {}),
         "gpu_launches": launches,

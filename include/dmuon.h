@@ -270,7 +270,10 @@ dmuon_status dmuon_set_weight_events(dmuon_plan_t plan, void* wait_before_write,
 /*
  * dmuon_read_device_status - synchronise stream, return the device status
  * bits accumulated since the last read (DMUON_DEV_*) in *bits, and clear
- * them. Returns DMUON_OK even when bits are set.
+ * them. Returns DMUON_OK even when bits are set. The word travels through a
+ * one-thread kernel into mapped page-locked host memory owned by the plan,
+ * not through a copy, so the read does not wait behind large transfers that
+ * other streams have in flight.
  */
 dmuon_status dmuon_read_device_status(dmuon_plan_t plan, void* stream, uint32_t* bits);
 

@@ -90,7 +90,6 @@ dmuon_status cuda_fail(cudaError_t e, const char* what) {
 constexpr int64_t kAlign = 1024;
 constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
 constexpr int64_t kSchedBytes = 128;   // one launch's tile-claim counters (own cache line)
-constexpr int64_t kPrefetchMaxBytes = 16LL << 20;  // largest operand set per matrix prefetched into L2
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -223,6 +222,10 @@ struct dmuon_plan_s {
   // With each resident pointer set, a TMA map of every W (tensor-core path, bf16 weights): the
   // last step's epilogue stores its updated W boxes through them. Pinned staging per slot.
   CUtensorMap* host_wmaps = nullptr;
+  // mapped page-locked word that dmuon_read_device_status reads the status into (host and device
+  // addresses)
+  unsigned* host_status = nullptr;
+  unsigned* host_status_dev = nullptr;
   std::vector<uint64_t> slot_ptrs[kPtrSlots];
   uint64_t slot_stamp[kPtrSlots] = {};
   uint64_t ptr_clock = 0;
@@ -685,20 +688,6 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
   if (vo.base != nullptr) {  // epilogue stores: 32 x 32 boxes staged with a 64-byte swizzle
     st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != DMUON_OK) return st;
-  }
-  // operands worth prefetching into L2 a wave ahead: a matrix's operands must be small next to
-  // the L2 (so that a wave of them plus the next fit), and every operand matrix is contiguous
-  // (one bucket slot) with a 16-byte multiple size
-  const int64_t op_bytes = va.mat_bytes + (opB != opA ? vb.mat_bytes : 0);
-  if (op_bytes <= kPrefetchMaxBytes) {
-    tb.pf_base[0] = va.base;
-    tb.pf_stride[0] = va.mat_bytes;
-    tb.pf_bytes[0] = va.mat_bytes / 16 * 16;
-    if (opB != opA) {
-      tb.pf_base[1] = vb.base;
-      tb.pf_stride[1] = vb.mat_bytes;
-      tb.pf_bytes[1] = vb.mat_bytes / 16 * 16;
-    }
   }
   tb.out = vo.base;
   tb.out_mat_stride = vo.mat_bytes;
@@ -1460,6 +1449,17 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
   if (test_hook("bind_staging")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_staging)");
   if (P->host_ptrs == nullptr && (e = cudaMallocHost(&P->host_ptrs, 8 * 3 * P->mats.size() * kPtrSlots)) != cudaSuccess)
     return cuda_fail(e, "cudaMallocHost");
+  if (P->host_status == nullptr) {
+    void* hs = nullptr;
+    if ((e = cudaHostAlloc(&hs, 64, cudaHostAllocMapped)) != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+    P->host_status = static_cast<unsigned*>(hs);
+  }
+  {  // its device address in this (possibly new) device's context
+    void* dp = nullptr;
+    if ((e = cudaHostGetDevicePointer(&dp, P->host_status, 0)) != cudaSuccess)
+      return cuda_fail(e, "cudaHostGetDevicePointer");
+    P->host_status_dev = static_cast<unsigned*>(dp);
+  }
   if (P->off_wmaps >= 0 && P->host_wmaps == nullptr &&
       (e = cudaMallocHost(&P->host_wmaps, sizeof(CUtensorMap) * P->mats.size() * kPtrSlots)) != cudaSuccess)
     return cuda_fail(e, "cudaMallocHost");
@@ -1624,13 +1624,15 @@ dmuon_status dmuon_read_device_status(dmuon_plan_t P, void* stream, uint32_t* bi
   if (P == nullptr || bits == nullptr) return fail(DMUON_ERR_INVALID_ARG, "NULL argument");
   if (P->ws == nullptr) return fail(DMUON_ERR_NOT_BOUND, "plan is not bound");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t v = 0;
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(&v, P->ws + P->off_status, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-    return cuda_fail(e, "status read");
+  // a one-thread kernel moves the word into mapped host memory and clears it (no copy engine, so
+  // the read does not wait behind other streams' transfers)
+  *reinterpret_cast<volatile unsigned*>(P->host_status) = 0u;
+  if ((e = launch_status_readout(reinterpret_cast<unsigned*>(P->ws + P->off_status), P->host_status_dev, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "status readout launch");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "status sync");
-  if ((e = cudaMemsetAsync(P->ws + P->off_status, 0, 4, s)) != cudaSuccess) return cuda_fail(e, "status clear");
-  *bits = v;
+  *bits = *reinterpret_cast<volatile unsigned*>(P->host_status);
   return DMUON_OK;
 }
 
@@ -1855,6 +1857,7 @@ void dmuon_plan_destroy(dmuon_plan_t P) {
   }
   if (P->host_ptrs) cudaFreeHost(P->host_ptrs);
   if (P->host_wmaps) cudaFreeHost(P->host_wmaps);
+  if (P->host_status) cudaFreeHost(P->host_status);
   delete P;
 }
 

@@ -82,11 +82,6 @@ struct TcBucket {
   int32_t out_ld, aux_ld;   // row pitch in elements
   int32_t m, n, kdim;
   int32_t pad;
-  // L2 prefetch of a matrix's operands one wave of tiles ahead (matrices whose operands are small
-  // enough, nullptr otherwise): base, bytes between matrices, bytes per matrix, per operand.
-  const char* pf_base[2];
-  int64_t pf_stride[2];
-  int64_t pf_bytes[2];
 };
 
 struct TcParams {
@@ -149,6 +144,8 @@ cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream
 cudaError_t launch_tc_pair(int phase, const TcParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
+// status word -> mapped host word (device address of it), then cleared
+cudaError_t launch_status_readout(unsigned* status, unsigned* host_out_dev, cudaStream_t s);
 // bind-time tuning only: bytes (a multiple of 16) of pseudo-random bf16 operands at dst
 cudaError_t launch_tuning_fill(void* dst, int64_t bytes, uint32_t seed, int grid, cudaStream_t s);
 

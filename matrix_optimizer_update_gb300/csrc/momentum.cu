@@ -335,6 +335,22 @@ cudaError_t launch_update0(const StreamParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ status readout
+// Copies the device status word to mapped, page-locked host memory and clears it. A kernel rather
+// than a copy: a copy of the word would queue on the copy engines behind whatever large transfers
+// other streams have in flight (a step's weights going back to the host, say).
+__global__ void status_readout_kernel(unsigned* status, volatile unsigned* host_out) {
+  const unsigned v = *status;
+  *status = 0u;
+  *host_out = v;
+  __threadfence_system();
+}
+
+cudaError_t launch_status_readout(unsigned* status, unsigned* host_out_dev, cudaStream_t s) {
+  status_readout_kernel<<<1, 1, 0, s>>>(status, host_out_dev);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ tuning data
 // Fills n bf16 elements (n a multiple of 8, dst 16-byte aligned) with values in [-1/64, 1/64) from a
 // counter-based hash of the element index: operands for bind-time tuning probes, so that the tensor

@@ -98,20 +98,6 @@ __device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int&
   return true;
 }
 
-// L2 prefetch of one matrix's operands (the planner sets them only for matrices whose operands
-// are small next to the L2), in pieces of 256 KB.
-constexpr int64_t kPrefetchPiece = 256 * 1024;
-__device__ __forceinline__ void prefetch_matrix(const TcBucket& B, int slot) {
-  for (int o = 0; o < 2; ++o) {
-    if (B.pf_base[o] == nullptr) continue;
-    const char* src = B.pf_base[o] + slot * B.pf_stride[o];
-    for (int64_t off = 0; off < B.pf_bytes[o]; off += kPrefetchPiece) {
-      const int64_t left = B.pf_bytes[o] - off;
-      ptx::bulk_prefetch_l2(src + off, static_cast<uint32_t>(left < kPrefetchPiece ? left : kPrefetchPiece));
-    }
-  }
-}
-
 // First output column of a symmetric-product tile (bucket, slot, ti, tj):
 // the planner lists each row block's tiles from its diagonal block on.
 template <int BN>
@@ -195,13 +181,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         if (w < 0) break;
         const int next = claim(j);  // its latency hides under this tile's loads
         const int4 it = p.items[w];
-        // The position one grid ahead is claimed about one wave of tiles later; if it starts a
-        // matrix with small operands, fetch that matrix's operands into L2 now (each matrix once:
-        // only the claimer of the position before it looks).
-        if (w + static_cast<int>(gridDim.x) < p.n_items) {
-          const int4 ahead = p.items[w + gridDim.x];
-          if (ahead.z == 0 && ahead.w == 0) prefetch_matrix(p.bk[ahead.x], ahead.y);
-        }
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         bool ok = true;
