@@ -685,6 +685,7 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
     st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bn);
   if (st != DMUON_OK) return st;
   tb.kdim = (phase == kPhaseGemm) ? B.m : va.inner;
+  tb.same_ab = (phase != kPhaseGemm && opA == opB) ? 1 : 0;
   if (vo.base != nullptr) {  // epilogue stores: 32 x 32 boxes staged with a 64-byte swizzle
     st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != DMUON_OK) return st;

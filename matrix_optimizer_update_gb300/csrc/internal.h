@@ -81,7 +81,8 @@ struct TcBucket {
   int64_t aux_mat_stride;
   int32_t out_ld, aux_ld;   // row pitch in elements
   int32_t m, n, kdim;
-  int32_t pad;
+  int32_t same_ab;  // both operands are the same matrix (X X^T, A A^T): a diagonal-start tile's A rows
+                    // are the first rows of its B rows
 };
 
 struct TcParams {

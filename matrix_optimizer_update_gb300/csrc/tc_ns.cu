@@ -98,6 +98,11 @@ __device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int&
   return true;
 }
 
+// A symmetric product of one matrix with itself (X X^T, A A^T): a tile that starts at its diagonal
+// block (tj = 0) has A rows 128 ti.. equal to the first 128 of its B rows, so the A operand is read
+// from the B stage and not loaded. (The same holds per CTA of a two-SM tile.)
+__device__ __forceinline__ bool a_rows_in_b(const TcBucket& B, const int4& it) { return B.same_ab && it.w == 0; }
+
 // First output column of a symmetric-product tile (bucket, slot, ti, tj):
 // the planner lists each row block's tiles from its diagonal block on.
 template <int BN>
@@ -183,15 +188,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
+        const bool a_in_b = a_rows_in_b(B, it);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(&sh->empty[stage], phase ^ 1u, abortf, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&sh->full[stage], kStageA + kStageB);
+          ptx::mbar_arrive_expect_tx(&sh->full[stage], (a_in_b ? 0u : kStageA) + kStageB);
           const int k0 = kb * kTcBK;
-          ptx::tma_load_3d(sA + stage * kStageA, &B.tmA, &sh->full[stage], k0, it.z * kTcBM, it.y);
+          if (!a_in_b) ptx::tma_load_3d(sA + stage * kStageA, &B.tmA, &sh->full[stage], k0, it.z * kTcBM, it.y);
           if (PHASE == kPhaseGemm) {
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
@@ -233,6 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         // left half (the first BN/2 rows of the B stage); the epilogue stores nothing of the rest.
         const uint32_t idesc =
             (PHASE != kPhaseGemm && BN == 256 && sym_col0<BN>(it) + BN / 2 >= B.m) ? idesc_half : idesc_full;
+        const bool a_in_b = a_rows_in_b(B, it);
         if (!ptx::mbar_wait(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns)) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + acc * BN;
@@ -242,8 +249,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sA + stage * kStageA);
           const uint32_t b0 = ptx::smem_u32(sB + stage * kStageB);
+          const uint32_t a0 = a_in_b ? b0 : ptx::smem_u32(sA + stage * kStageA);
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
             // K-major 128B-swizzled rows: a K step of 16 bf16 is 32 bytes inside the swizzle atom;

@@ -107,16 +107,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
+        // a diagonal pair tile of a matrix with itself: each CTA's A rows are its B rows
+        const bool a_in_b = PHASE != kPhaseGemm && B.same_ab && it.w == 0;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_cluster(&sh->empty[stage], phase ^ 1u, abortf, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
-          if (leader) ptx::mbar_arrive_expect_tx(&sh->full[stage], 2 * (kHalfA + kHalfB));
+          if (leader) ptx::mbar_arrive_expect_tx(&sh->full[stage], 2 * ((a_in_b ? 0u : kHalfA) + kHalfB));
           const uint32_t fb = lead_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
           const int k0 = kb * kTcBK;
-          ptx::tma_load_3d_pair(sA + stage * kHalfA, &B.tmA, fb, k0, it.z * kPairBM + rank * 128, it.y);
+          if (!a_in_b)
+            ptx::tma_load_3d_pair(sA + stage * kHalfA, &B.tmA, fb, k0, it.z * kPairBM + rank * 128, it.y);
           if (PHASE == kPhaseGemm) {
 #pragma unroll
             for (int q = 0; q < 2; ++q)
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         const uint32_t acc = local & 1u;
+        const bool a_in_b = PHASE != kPhaseGemm && B.same_ab && it.w == 0;
         if (!ptx::mbar_wait_cluster(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns))
           break;
         ptx::tc_fence_after();
@@ -165,8 +169,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sA + stage * kHalfA);
           const uint32_t b0 = ptx::smem_u32(sB + stage * kHalfB);
+          const uint32_t a0 = a_in_b ? b0 : ptx::smem_u32(sA + stage * kHalfA);
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
             const uint64_t adesc = ptx::sw128_desc(a0 + kk * 32, 16, 1024);
