@@ -738,6 +738,8 @@ void destroy_events(dmuon_plan_s& P) {
 // section 2.4: tile shapes, block sizes and pipeline depths are searched and
 // the chosen configuration is cached and reused).
 constexpr int kTuneCands = 3;  // 0: one-SM 128 wide, 1: one-SM 256 wide, 2: two-SM 256 x 256
+constexpr double kTuneHeatMs = 150.0, kTuneTimedMs = 150.0;  // per configuration and kind of product
+constexpr double kTuneMargin = 0.05;  // a configuration other than the default must be this much cheaper
 constexpr int kTuneCandBn[kTuneCands] = {128, 256, 256};
 
 struct TuneKey {
@@ -833,9 +835,9 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         auto launch = [&]() {
           return T.pair ? launch_tc_pair(phase, tp, grid, s) : launch_tc(phase, T.bn_sym, tp, grid, s);
         };
-        // Timed long enough for the clock to settle under the power limit: about 30 ms untimed,
-        // then about 60 ms timed. A configuration that does more work per clock but draws more
-        // power is then measured at the clock it gets in a long step, not at an idle GPU's clock.
+        // Timed long enough for the clock to settle under the power limit: about 150 ms untimed,
+        // then about 150 ms timed. A configuration that does more work per clock but draws more
+        // power is then measured closer to the clock it gets in a long step than to an idle GPU's.
         auto run = [&](int reps, float* ms) -> cudaError_t {
           cudaError_t r = cudaEventRecord(e0, s);
           for (int rep = 0; rep < reps && r == cudaSuccess; ++rep) r = launch();
@@ -847,8 +849,8 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         float ms = 0.f;
         e = run(1, &ms);  // also the first launch of this kernel
         const double per = std::max(ms, 0.01f);
-        if (e == cudaSuccess) e = run(static_cast<int>(std::min(400.0, std::ceil(30.0 / per))), &ms);
-        const int reps = static_cast<int>(std::min(400.0, std::max(3.0, std::ceil(60.0 / per))));
+        if (e == cudaSuccess) e = run(static_cast<int>(std::min(2000.0, std::ceil(kTuneHeatMs / per))), &ms);
+        const int reps = static_cast<int>(std::min(2000.0, std::max(3.0, std::ceil(kTuneTimedMs / per))));
         if (e == cudaSuccess) e = run(reps, &ms);
         if (e != cudaSuccess) {
           st = cuda_fail(e, "tuning run");
@@ -886,8 +888,17 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
       cg[ci] = tiles.size() * n_gm * tt.sm_ms[ci][2];
     }
     for (int ci = 0; ci < kTuneCands; ++ci) B.tune_cost[ci] = cs[ci] + cg[ci] < 1e299 ? cs[ci] + cg[ci] : 0.0;
-    const int bs = cs[0] <= cs[1] ? 0 : 1, bg = cg[0] <= cg[1] ? 0 : 1;  // best one-SM widths
-    if (cs[2] + cg[2] < cs[bs] + cg[bg]) {
+    // Best one-SM widths, then pairs against them. A configuration other than the planner's default
+    // must be cheaper by kTuneMargin: what a probe gains per clock, a long step under the power limit
+    // partly gives back in clock (measured: pairs chosen on a 2 % probe advantage lost 5 % on MoE).
+    const int dsym = B.bn_sym == 128 ? 0 : 1, dgem = B.bn_gemm == 128 ? 0 : 1;  // the default widths
+    const int bs = cs[1 - dsym] * (1.0 + kTuneMargin) < cs[dsym] ? 1 - dsym : dsym;
+    const int bg = cg[1 - dgem] * (1.0 + kTuneMargin) < cg[dgem] ? 1 - dgem : dgem;
+    const double best_one = cs[bs] + cg[bg], dflt = cs[dsym] + cg[dgem];
+    const bool dflt_pair = B.pair;
+    const double pair_cost = cs[2] + cg[2];
+    if (dflt_pair ? !(best_one * (1.0 + kTuneMargin) < pair_cost)
+                  : (pair_cost * (1.0 + kTuneMargin) < dflt && pair_cost < best_one)) {
       B.pair = true;
       B.bn_sym = B.bn_gemm = 256;
       for (int k = 0; k < 3; ++k) B.tile_ms[k] = tt.sm_ms[2][k];
