@@ -257,3 +257,31 @@ def test_polynomial_coefficients_per_launch(ax):
             assert L["diag"] == 0.0
         else:
             assert L["kind"] == dm.KIND_GRAM and L["a"] == 0.0 and L["diag"] == 0.0
+
+
+@pytest.mark.parametrize("name", ["qwen2.5-1.5b", "moe-16x64"])
+def test_workspace_regions_are_disjoint_and_do_not_depend_on_tiling(name):
+    """The regions describe lists lie inside the workspace and do not overlap; and the layout is the
+    same whatever the tile configuration (the tuner re-plans tile widths and pairs after the caller
+    has sized the workspace, so nothing may move with them)."""
+    w = wl.get(name)
+    plans = [dm.dmuon_plan(w.shapes, w.ns_steps, flags=f)
+             for f in (0, dm.FLAG_PAIR_TILES, dm.FLAG_TUNE, dm.FLAG_STATIC_TILES)]
+    descs = [p.describe() for p in plans]
+    for p, d in zip(plans, descs):
+        regs = [d["regions"]["status"]] + d["regions"]["tables"] + d["regions"]["scratch"]
+        regs = sorted((o, o + n) for o, n in regs)
+        assert regs[0][0] >= 0 and regs[-1][1] <= p.workspace_bytes()
+        for (a0, a1), (b0, b1) in zip(regs, regs[1:]):
+            assert a1 <= b0, (a0, a1, b0, b1)
+    assert all(d["regions"] == descs[0]["regions"] for d in descs)
+    assert len({p.workspace_bytes() for p in plans}) == 1
+
+
+def test_many_tile_configurations_keep_the_layout():
+    # 19 buckets whose default widths differ: each could become a launch chunk of its own
+    shapes = [(16 * (k + 1), 256 + 64 * k) for k in range(19)]
+    a = dm.dmuon_plan(shapes, 3)
+    b = dm.dmuon_plan(shapes, 3, flags=dm.FLAG_PAIR_TILES | dm.FLAG_TUNE)
+    assert a.describe()["regions"] == b.describe()["regions"]
+    assert a.workspace_bytes() == b.workspace_bytes()
