@@ -672,21 +672,17 @@ View view_of(const dmuon_plan_s& P, const BucketPlan& B, int role) {
 
 // Operand maps and epilogue pointers of one bucket for one tensor-core launch.
 dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phase, int bn, int opA, int opB,
-                            int out, int aux, TcBucket& tb, bool pair) {
-  // K width of a ring stage: 32 (64-byte rows, 64-byte swizzle) for the one-SM kernel, 64 (128-byte
-  // rows) for CTA pairs; the MN-major X operand of the gemm keeps 128-byte rows (64 columns) either way
-  const int bk = pair ? kPairBK : kTcBK;
-  const CUtensorMapSwizzle kswz = bk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+                            int out, int aux, TcBucket& tb) {
   tb.slot_mat = reinterpret_cast<const int32_t*>(P.ws + B.off_slotmat);
   tb.m = B.m;
   tb.n = B.n;
   const View va = view_of(P, B, opA), vb = view_of(P, B, opB), vo = view_of(P, B, out), vx = view_of(P, B, aux);
-  dmuon_status st = make_map(&tb.tmA, va.base, va.inner, va.rows, B.count, va.ld, bk, kTcBM, kswz);
+  dmuon_status st = make_map(&tb.tmA, va.base, va.inner, va.rows, B.count, va.ld, 64, kTcBM);
   if (st != DMUON_OK) return st;
-  if (phase == kPhaseGemm)  // the m x n operand, MN-major: 64 columns x bk rows per box
-    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bk);
+  if (phase == kPhaseGemm)  // the m x n operand, MN-major: 64 columns x 64 rows per box
+    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, 64);
   else
-    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, bk, bn, kswz);
+    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bn);
   if (st != DMUON_OK) return st;
   tb.kdim = (phase == kPhaseGemm) ? B.m : va.inner;
   tb.same_ab = (phase != kPhaseGemm && opA == opB) ? 1 : 0;
@@ -821,8 +817,7 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         TcParams tp;
         std::memset(&tp, 0, sizeof(tp));
         // a pair's CTAs each load 128 rows of a K-major B operand
-        if ((st = fill_tc_bucket(P, T, phase, T.pair ? 128 : T.bn_sym, opA, opB, out, aux, tp.bk[0], T.pair)) !=
-            DMUON_OK)
+        if ((st = fill_tc_bucket(P, T, phase, T.pair ? 128 : T.bn_sym, opA, opB, out, aux, tp.bk[0])) != DMUON_OK)
           break;
         tp.items = probe;
         tp.n_items = n;
@@ -1394,8 +1389,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
         const BucketPlan& B = P->buckets[ch[lb]];
         // a pair's CTAs each load 128 rows of a K-major B operand
         if (test_hook("bind_maps")) return fail(DMUON_ERR_CUDA, "injected failure (DMUON_TEST_FAIL=bind_maps)");
-        dmuon_status st =
-            fill_tc_bucket(*P, B, L.phase, L.pair ? 128 : L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb], L.pair);
+        dmuon_status st = fill_tc_bucket(*P, B, L.phase, L.pair ? 128 : L.bn, L.opA, L.opB, L.out, L.aux, tp.bk[lb]);
         if (st != DMUON_OK) return st;
       }
       tp.items = items + lr.first;

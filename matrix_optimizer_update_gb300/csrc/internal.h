@@ -16,8 +16,7 @@ constexpr int kMaxBucketsPerLaunch = 7;  // 7 x 512 B of bucket descriptors fit 
 // bucket), K staged 64 at a time.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;  // default tile width
-constexpr int kTcBK = 32;    // K width of a ring stage of the one-SM kernel (64-byte swizzled rows)
-constexpr int kPairBK = 64;  // K width of a ring stage of the two-SM kernel (128-byte swizzled rows)
+constexpr int kTcBK = 64;
 constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 epilogue
 
 // fp32 SIMT tile.

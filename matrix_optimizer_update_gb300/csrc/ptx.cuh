@@ -195,20 +195,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
   for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
 }
 
-// Shared-memory matrix descriptor, sm_100-family format: start address, leading- and
-// stride-dimension byte offsets (all >> 4), descriptor version 1 at bit 46, layout type in bits
-// 61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= static_cast<uint64_t>(layout & 7u) << 61;
-  return d;
-}
-constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4;
-
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100-family format:
 // start address, leading- and stride-dimension byte offsets (all >> 4),
 // descriptor version 1 at bit 46, swizzle mode 2 (128B) in bits 61-63.

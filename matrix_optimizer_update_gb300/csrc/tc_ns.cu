@@ -52,22 +52,17 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 8 KB: 128 rows x 64 B (K-major, 64-byte swizzle)
-constexpr uint32_t kKRowBytes = kTcBK * 2;         // bytes of one K-major operand row in a stage
-constexpr uint32_t kLayoutK = kKRowBytes == 128 ? ptx::kLayoutSw128 : ptx::kLayoutSw64;
-constexpr uint32_t kRingBytes = 192 * 1024;        // operand ring: 8 stages at 256 wide, 12 at 128
+constexpr uint32_t kStageA = kTcBM * kTcBK * 2;  // 16 KB: 128 rows x 128 B
 constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
 using epi::kStageBox;
 
 // Tile width N of one CTA (the UMMA N): 256, or 128 where the planner's
 // tile-count cost favours it. Shared-memory stages fill the same 192 KB
 // either way; 32 KB of epilogue staging and 1 KB of barriers follow them.
-// A stage holds K = 32: more, smaller stages keep more bytes in flight than
-// 64-wide ones in the same shared memory (7 of 8 stages can be loading).
 template <int BN>
 struct TcCfg {
-  static constexpr uint32_t kStageB = BN * kTcBK * 2;  // BN rows x 64 B (or BN/64 x [32 k-rows x 128 B])
-  static constexpr int kStages = kRingBytes / (kStageA + kStageB);
+  static constexpr uint32_t kStageB = BN * kTcBK * 2;  // BN rows x 128 B (or BN/64 x [64 k-rows x 128 B])
+  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr uint32_t kTmemCols = 2 * BN;        // two fp32 accumulators of BN columns
   static constexpr int kEpiChunks = BN / 2 / 32;       // 32-column chunks per epilogue warp
 };
@@ -90,7 +85,7 @@ struct TcShared {
   int abort_flag;
 };
 
-static_assert(sizeof(TcShared<12>) <= 1024, "barriers must fit their 1 KB");
+static_assert(sizeof(TcShared<6>) <= 1024, "barriers must fit their 1 KB");
 
 // Consumer side of the item ring: the j-th item of this CTA (false when the CTA gives up).
 template <int STAGES>
@@ -206,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           if (PHASE == kPhaseGemm) {
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
-              ptx::tma_load_3d(sB + stage * kStageB + q * (64 * kKRowBytes), &B.tmB, &sh->full[stage],
+              ptx::tma_load_3d(sB + stage * kStageB + q * (64 * kTcBK * 2), &B.tmB, &sh->full[stage],
                                it.w * BN + q * 64, k0, it.y);
           } else {  // rows of the tile's columns; rows past the matrix's edge are zero-filled
             ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, sym_col0<BN>(it), it.y);
@@ -258,16 +253,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           const uint32_t a0 = a_in_b ? b0 : ptx::smem_u32(sA + stage * kStageA);
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
-            // K-major swizzled rows of kKRowBytes: a K step of 16 bf16 is 32 bytes inside the
-            // swizzle atom; 8-row groups are 8 * kKRowBytes apart.
-            const uint64_t adesc = ptx::smem_desc(a0 + kk * 32, 16, 8 * kKRowBytes, kLayoutK);
+            // K-major 128B-swizzled rows: a K step of 16 bf16 is 32 bytes inside the swizzle atom;
+            // 8-row groups are 1024 bytes apart.
+            const uint64_t adesc = ptx::sw128_desc(a0 + kk * 32, 16, 1024);
             uint64_t bdesc;
             if (PHASE == kPhaseGemm) {
-              // MN-major, 128-byte swizzle: 64-column chunks of kTcBK k-rows (leading), 8 k-rows
-              // 1024 B apart (stride); a K step of 16 rows is 2048 bytes.
-              bdesc = ptx::smem_desc(b0 + kk * 2048, 64 * kKRowBytes, 1024, ptx::kLayoutSw128);
+              // MN-major: 64-column chunks 8 KB apart (leading), 8 k-rows 1024 B apart (stride);
+              // a K step of 16 rows is 2048 bytes.
+              bdesc = ptx::sw128_desc(b0 + kk * 2048, 64 * kTcBK * 2, 1024);
             } else {
-              bdesc = ptx::smem_desc(b0 + kk * 32, 16, 8 * kKRowBytes, kLayoutK);
+              bdesc = ptx::sw128_desc(b0 + kk * 32, 16, 1024);
             }
             ptx::umma_f16(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }

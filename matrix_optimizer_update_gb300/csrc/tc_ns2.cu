@@ -37,8 +37,8 @@ using bf16 = __nv_bfloat16;
 
 constexpr int kPairBM = 256;                   // rows of a pair tile (128 per CTA)
 constexpr int kPairBN = 256;                   // columns of a pair tile
-constexpr uint32_t kHalfA = 128 * kPairBK * 2;   // 16 KB: this CTA's 128 rows of A
-constexpr uint32_t kHalfB = 128 * kPairBK * 2;   // 16 KB: this CTA's half of B
+constexpr uint32_t kHalfA = 128 * kTcBK * 2;   // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t kHalfB = 128 * kTcBK * 2;   // 16 KB: this CTA's half of B
 constexpr int kStages = 6;
 constexpr uint32_t kTmemCols = 2 * kPairBN;    // two 128 x 256 fp32 accumulators per CTA
 constexpr int kEpiWarps = 8;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       for (int w = pair; w < p.n_items; w += npairs) {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
-        const int nk = (B.kdim + kPairBK - 1) / kPairBK;
+        const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         // a diagonal pair tile of a matrix with itself: each CTA's A rows are its B rows
         const bool a_in_b = PHASE != kPhaseGemm && B.same_ab && it.w == 0;
         bool ok = true;
@@ -117,13 +117,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
           }
           if (leader) ptx::mbar_arrive_expect_tx(&sh->full[stage], 2 * ((a_in_b ? 0u : kHalfA) + kHalfB));
           const uint32_t fb = lead_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
-          const int k0 = kb * kPairBK;
+          const int k0 = kb * kTcBK;
           if (!a_in_b)
             ptx::tma_load_3d_pair(sA + stage * kHalfA, &B.tmA, fb, k0, it.z * kPairBM + rank * 128, it.y);
           if (PHASE == kPhaseGemm) {
 #pragma unroll
             for (int q = 0; q < 2; ++q)
-              ptx::tma_load_3d_pair(sB + stage * kHalfB + q * (64 * kPairBK * 2), &B.tmB, fb,
+              ptx::tma_load_3d_pair(sB + stage * kHalfB + q * (64 * kTcBK * 2), &B.tmB, fb,
                                     it.w * kPairBN + rank * 128 + q * 64, k0, it.y);
           } else {  // symmetric products list a row pair's tiles from its diagonal block on
             ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, (it.z + it.w) * kPairBN + rank * 128, it.y);
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       for (int w = pair; w < p.n_items && ok; w += npairs, ++local) {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
-        const int nk = (B.kdim + kPairBK - 1) / kPairBK;
+        const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         const uint32_t acc = local & 1u;
         const bool a_in_b = PHASE != kPhaseGemm && B.same_ab && it.w == 0;
         if (!ptx::mbar_wait_cluster(&sh->tempty[acc], ((local >> 1) & 1u) ^ 1u, abortf, p.status, p.timeout_ns))
@@ -172,9 +172,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
           const uint32_t b0 = ptx::smem_u32(sB + stage * kHalfB);
           const uint32_t a0 = a_in_b ? b0 : ptx::smem_u32(sA + stage * kHalfA);
 #pragma unroll
-          for (int kk = 0; kk < kPairBK / 16; ++kk) {
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
             const uint64_t adesc = ptx::sw128_desc(a0 + kk * 32, 16, 1024);
-            const uint64_t bdesc = (PHASE == kPhaseGemm) ? ptx::sw128_desc(b0 + kk * 2048, 64 * kPairBK * 2, 1024)
+            const uint64_t bdesc = (PHASE == kPhaseGemm) ? ptx::sw128_desc(b0 + kk * 2048, 64 * kTcBK * 2, 1024)
                                                          : ptx::sw128_desc(b0 + kk * 32, 16, 1024);
             ptx::umma_f16_pair(d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
