@@ -313,7 +313,11 @@ dmuon_status build_plan(dmuon_plan_s& P) {
   P.xel = P.tc ? 2 : 4;
   P.tile_m = P.tc ? kTcBM : kSimtBM;
   P.tile_n = P.tc ? kTcBN : kSimtBN;
-  const int ld_mult = P.tc ? 8 : 4;
+  // Row pitch of the m x n iterates: tensor-core buckets round n up to 64 elements, so that the
+  // gemm's 4-D view of X (64-column chunks of a row) never reads past a row; m x m buffers and the
+  // fp32 path round to 16 bytes (TMA strides)
+  const int ld_mult = P.tc ? 64 : 4;
+  const int m_ld_mult = P.tc ? 8 : 4;
 
   // ---- buckets by (short, long) shape, most expensive first
   std::map<std::pair<int, int>, int> key;
@@ -335,7 +339,7 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].m = order[b].first;
     P.buckets[b].n = order[b].second;
     P.buckets[b].x_ld = static_cast<int32_t>(align_up(order[b].second, ld_mult));
-    P.buckets[b].m_ld = static_cast<int32_t>(align_up(order[b].first, ld_mult));
+    P.buckets[b].m_ld = static_cast<int32_t>(align_up(order[b].first, m_ld_mult));
     // the Gram-space form pays (>= 26% fewer flops) and keeps bf16 accuracy on wide matrices only
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
@@ -367,7 +371,7 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     B.n_transposed += d.transposed;
     d.x_ld = B.x_ld;
     d.scale = static_cast<float>(std::sqrt(std::max(1.0, static_cast<double>(r) / c)));
-    d.flat = (!d.transposed && c % 8 == 0) ? 1 : 0;
+    d.flat = (!d.transposed && c % 8 == 0 && d.x_ld == c) ? 1 : 0;  // U rows land contiguous
     d.tiles_c = static_cast<int32_t>(cdiv(c, kTileC));
     d.vec_ok = (c % 4 == 0) ? 1 : 0;
     d.unit_begin = units;
@@ -627,6 +631,26 @@ dmuon_status make_map(CUtensorMap* map, const void* base, int inner, int rows, i
   return DMUON_OK;
 }
 
+// The MN-major m x n operand of the gemm (rows of ld elements, ld a multiple of 64) as a 4-D map
+// [count][chunk of 64 columns][row][64 columns], so that one box {64, 64 rows, chunks} brings a
+// whole 64-row slab of chunks x 64 columns in one copy, each 64-column chunk an 8 KB block of
+// 128-byte swizzled rows. Columns past n inside the last chunk read the row's padding (they feed
+// only output columns past n, which are never stored); chunks past the last are zero fill.
+dmuon_status make_map_mn(CUtensorMap* map, const void* base, int rows, int count, int ld_elems, int chunks_per_box) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (ld_elems % 64 != 0) return fail(DMUON_ERR_INVALID_ARG, "internal: MN-major row pitch %d not a multiple of 64", ld_elems);
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(ld_elems / 64), (cuuint64_t)count};
+  cuuint64_t strides[3] = {(cuuint64_t)ld_elems * 2, 128, (cuuint64_t)ld_elems * 2 * rows};
+  cuuint32_t box[4] = {64, 64, (cuuint32_t)chunks_per_box, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled failed for a 4-D operand (%d)", (int)r);
+  return DMUON_OK;
+}
+
 // W (rows x cols bf16, row-major) as a 2-D map of 32 x 32 boxes with the 64-byte swizzle, for
 // the TMA stores of the last step's W update. All zeros when the row pitch is not a multiple of
 // 16 bytes: the kernels then update that W row by row and never use the map.
@@ -679,8 +703,8 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
   const View va = view_of(P, B, opA), vb = view_of(P, B, opB), vo = view_of(P, B, out), vx = view_of(P, B, aux);
   dmuon_status st = make_map(&tb.tmA, va.base, va.inner, va.rows, B.count, va.ld, 64, kTcBM);
   if (st != DMUON_OK) return st;
-  if (phase == kPhaseGemm)  // the m x n operand, MN-major: 64 columns x 64 rows per box
-    st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, 64);
+  if (phase == kPhaseGemm)  // the m x n operand, MN-major: bn/64 chunks of 64 columns x 64 rows per box
+    st = make_map_mn(&tb.tmB, vb.base, vb.rows, B.count, vb.ld, bn / 64);
   else
     st = make_map(&tb.tmB, vb.base, vb.inner, vb.rows, B.count, vb.ld, 64, bn);
   if (st != DMUON_OK) return st;

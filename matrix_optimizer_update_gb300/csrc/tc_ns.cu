@@ -198,11 +198,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           ptx::mbar_arrive_expect_tx(&sh->full[stage], (a_in_b ? 0u : kStageA) + kStageB);
           const int k0 = kb * kTcBK;
           if (!a_in_b) ptx::tma_load_3d(sA + stage * kStageA, &B.tmA, &sh->full[stage], k0, it.z * kTcBM, it.y);
-          if (PHASE == kPhaseGemm) {
-#pragma unroll
-            for (int q = 0; q < BN / 64; ++q)
-              ptx::tma_load_3d(sB + stage * kStageB + q * (64 * kTcBK * 2), &B.tmB, &sh->full[stage],
-                               it.w * BN + q * 64, k0, it.y);
+          if (PHASE == kPhaseGemm) {  // one copy: BN/64 chunks of 64 columns x 64 k-rows, 8 KB apart
+            ptx::tma_load_4d(sB + stage * kStageB, &B.tmB, &sh->full[stage], 0, k0, it.w * (BN / 64), it.y);
           } else {  // rows of the tile's columns; rows past the matrix's edge are zero-filled
             ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, sym_col0<BN>(it), it.y);
           }

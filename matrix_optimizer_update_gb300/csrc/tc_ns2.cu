@@ -120,11 +120,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
           const int k0 = kb * kTcBK;
           if (!a_in_b)
             ptx::tma_load_3d_pair(sA + stage * kHalfA, &B.tmA, fb, k0, it.z * kPairBM + rank * 128, it.y);
-          if (PHASE == kPhaseGemm) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-              ptx::tma_load_3d_pair(sB + stage * kHalfB + q * (64 * kTcBK * 2), &B.tmB, fb,
-                                    it.w * kPairBN + rank * 128 + q * 64, k0, it.y);
+          if (PHASE == kPhaseGemm) {  // one copy: this CTA's two 64-column chunks of 64 k-rows
+            ptx::tma_load_4d_pair(sB + stage * kHalfB, &B.tmB, fb, 0, k0, (it.w * kPairBN + rank * 128) / 64, it.y);
           } else {  // symmetric products list a row pair's tiles from its diagonal block on
             ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, (it.z + it.w) * kPairBN + rank * 128, it.y);
           }
