@@ -710,11 +710,8 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
   if (st != DMUON_OK) return st;
   tb.kdim = (phase == kPhaseGemm) ? B.m : va.inner;
   tb.same_ab = (phase != kPhaseGemm && opA == opB) ? 1 : 0;
-  if (vo.base != nullptr) {  // epilogue stores: X' in 32 x 64 boxes (128-byte swizzle), symmetric
-                             // products in 32 x 32 boxes (64-byte swizzle)
-    st = phase == kPhaseGemm
-             ? make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B)
-             : make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (vo.base != nullptr) {  // epilogue stores: 32 x 32 boxes staged with a 64-byte swizzle
+    st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != DMUON_OK) return st;
   }
   tb.out = vo.base;

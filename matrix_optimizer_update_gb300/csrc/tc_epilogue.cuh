@@ -91,21 +91,6 @@ __device__ __forceinline__ void stage_row_sw64(uint8_t* box, int r, const float 
   }
 }
 
-// X' of the gemm goes out two chunks at a time: a 32 x 64 box of 128-byte rows with the 128-byte
-// swizzle (16-byte piece c of row r at piece c ^ (r & 7)); lane r's chunk `half` fills pieces
-// 4 half .. 4 half + 3 of row r.
-__device__ __forceinline__ void stage_row_sw128_half(uint8_t* box, int r, int half, const float (&v)[32]) {
-  uint8_t* row = box + r * 128;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
-    *reinterpret_cast<uint4*>(row + (((4 * half + q) ^ (r & 7)) << 4)) = u;
-  }
-}
-
 // The transpose: lane r's value k goes to row k, column r, so that the box
 // stored at (x = row origin, y = column origin) is the mirror image.
 __device__ __forceinline__ void stage_col_sw64(uint8_t* box, int r, const float (&v)[32]) {
@@ -420,13 +405,13 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const TcBucket
 // each chunk is drained and written: through a staged TMA box (X', symmetric
 // chunks above the diagonal, with the mirror image), through the staged W
 // update, or per row (diagonal chunks, matrix edges, fp32 weights, a*X in
-// the epilogue). stg: this warp's two staging boxes (4 KB), which also hold two X' chunks as
-// one 32 x 64 box.
+// the epilogue). stg: this warp's two staging boxes; nbox counts the X' boxes
+// (their double buffering spans tiles).
 constexpr int kStageBox = 32 * 32 * 2;  // one 32 x 32 bf16 box staged for a TMA store
 
 template <int PHASE, int kChunks, class WaitAcc>
 __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket& B, const int4& it, int i0, int jbase,
-                                              uint32_t tbase, int lane, uint8_t* stg,
+                                              uint32_t tbase, int lane, uint8_t* stg, uint32_t& nbox,
                                               WaitAcc&& wait_acc) {
   const int i = i0 + lane;
   // The linear term's operand does not depend on the accumulator: the first
@@ -497,22 +482,17 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const TcBucket&
     if (PHASE == kPhaseGemm && gemm_tma) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) v[k] *= sc;
-      // two chunks per TMA store (one op for 4 KB): the pair's first chunk waits until the store
-      // that last read the staging (the previous pair's, possibly of the previous tile) is done
-      if ((ch & 1) == 0) {
-        if (lane == 0) ptx::bulk_wait_read<0>();
-        __syncwarp();
+      uint8_t* box = stg + (nbox & 1u) * kStageBox;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this box is done with it
+      __syncwarp();
+      stage_row_sw64(box, lane, v);
+      ptx::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (i0 < B.m && j0 < B.n) ptx::tma_store_3d(&B.tmOut, box, j0, i0, it.y);
+        ptx::bulk_commit();  // one group per box, stored or not, so the count above holds
       }
-      stage_row_sw128_half(stg, lane, ch & 1, v);
-      if ((ch & 1) == 1 || ch == kChunks - 1) {
-        ptx::fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          const int jp = j0 - 32 * (ch & 1);  // the pair's first column
-          if (i0 < B.m && jp < B.n) ptx::tma_store_3d(&B.tmOut, stg, jp, i0, it.y);
-          ptx::bulk_commit();
-        }
-      }
+      ++nbox;
     } else if (PHASE == kPhaseGemm && w_last) {
       uint8_t* box = stg + (ch & 1) * kStageBox;
       ptx::cp_async_wait<1>();  // this chunk's copies (all but the newest group) have landed

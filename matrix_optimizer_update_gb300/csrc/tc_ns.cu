@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
-    uint32_t local = 0;
+    uint32_t local = 0, nbox = 0;
     for (;; ++local) {
       int w = -2;  // -2: the CTA gave up
       if (lane == 0 && !ring_take(sh, local, w, abortf, p)) w = -2;
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       const int i0 = it.z * kTcBM + q * 32;
       const int jbase = (PHASE == kPhaseGemm ? it.w * BN : sym_col0<BN>(it)) + half * (BN / 2);
       const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
-      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, [&]() {
+      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
         return ptx::mbar_wait(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);
       });
       if (!ok) break;

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
     const int half = (warp - 2) >> 2;
     const uint32_t lead_tempty = ptx::mapa_shared(ptx::smem_u32(&sh->tempty[0]), 0);
     uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
-    uint32_t local = 0;
+    uint32_t local = 0, nbox = 0;
     for (int w = pair; w < p.n_items; w += npairs, ++local) {
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       const int i0 = it.z * kPairBM + static_cast<int>(rank) * 128 + q * 32;
       const int jbase = (PHASE == kPhaseGemm ? it.w : it.z + it.w) * kPairBN + half * (kPairBN / 2);
       const uint32_t tbase = tmem + acc * kPairBN + half * (kPairBN / 2) + ((uint32_t)(q * 32) << 16);
-      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, [&]() {
+      const bool ok = epi::epilogue_tile<PHASE, kEpiChunks>(p, B, it, i0, jbase, tbase, lane, stg, nbox, [&]() {
         return ptx::mbar_wait_cluster(&sh->tfull[acc], (local >> 1) & 1u, abortf, p.status, p.timeout_ns);
       });
       if (!ok) break;
