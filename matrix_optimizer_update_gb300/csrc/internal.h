@@ -72,7 +72,8 @@ struct StreamParams {
 // One bucket as seen by a tensor-core launch.
 struct TcBucket {
   CUtensorMap tmA;  // A operand: 128 x 64 boxes, K-major
-  CUtensorMap tmB;  // B operand: 256 x 64 boxes K-major (gram/poly) or 64 x 64 boxes MN-major (gemm)
+  CUtensorMap tmB;  // B operand: 256 x 64 boxes K-major (gram/poly), or for the gemm a 4-D map that brings
+                    // BN/64 chunks of 64 columns x 64 k-rows in one copy (MN-major)
   CUtensorMap tmOut;  // output: 32 x 32 boxes, 64-byte swizzle (epilogue TMA stores)
   const int32_t* slot_mat;  // slot -> global matrix index
   char* out;                // A (gram), B (poly), X_{k+1} (gemm, not last)
