@@ -90,7 +90,6 @@ dmuon_status cuda_fail(cudaError_t e, const char* what) {
 constexpr int64_t kAlign = 1024;
 constexpr int64_t kProbeTiles = 4096;  // tile-list room of one tuning probe
 constexpr int64_t kSchedBytes = 128;   // one launch's tile-claim counters (own cache line)
-constexpr int64_t kPrefetchMaxBytes = 16LL << 20;  // largest operand set per matrix prefetched into L2
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -714,16 +713,6 @@ dmuon_status fill_tc_bucket(const dmuon_plan_s& P, const BucketPlan& B, int phas
   if (vo.base != nullptr) {  // epilogue stores: 32 x 32 boxes staged with a 64-byte swizzle
     st = make_map(&tb.tmOut, vo.base, vo.inner, vo.rows, B.count, vo.ld, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != DMUON_OK) return st;
-  }
-  // operands worth an L2 prefetch one wave ahead: a matrix's operands small next to the L2, so that
-  // a wave's worth of them and the next fit beside what the running tiles read
-  if (va.mat_bytes + (opB != opA ? vb.mat_bytes : 0) <= kPrefetchMaxBytes) {
-    tb.pf_a = va.base;
-    tb.pf_a_stride = va.mat_bytes;
-    tb.pf_a_ld = va.ld * 2;
-    tb.pf_b = vb.base;
-    tb.pf_b_stride = vb.mat_bytes;
-    tb.pf_b_ld = vb.ld * 2;
   }
   tb.out = vo.base;
   tb.out_mat_stride = vo.mat_bytes;

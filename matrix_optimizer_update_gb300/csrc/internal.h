@@ -84,12 +84,6 @@ struct TcBucket {
   int32_t m, n, kdim;
   int32_t same_ab;  // both operands are the same matrix (X X^T, A A^T): a diagonal-start tile's A rows
                     // are the first rows of its B rows
-  // Operands for the L2 prefetch one wave of tiles ahead, set only for matrices whose operands are
-  // small next to the L2 (nullptr otherwise): base, bytes between matrices, row pitch in bytes.
-  const char* pf_a;
-  const char* pf_b;
-  int64_t pf_a_stride, pf_b_stride;
-  int32_t pf_a_ld, pf_b_ld;
 };
 
 struct TcParams {

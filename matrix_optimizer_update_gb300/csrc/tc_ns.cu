@@ -103,42 +103,6 @@ __device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int&
 // from the B stage and not loaded. (The same holds per CTA of a two-SM tile.)
 __device__ __forceinline__ bool a_rows_in_b(const TcBucket& B, const int4& it) { return B.same_ab && it.w == 0; }
 
-// L2 prefetch, by the 256 epilogue threads, of the operand lines that tile `a` (claimed about one
-// wave of tiles after this CTA's current one) is the first in list order to read: for a symmetric
-// product the B rows of a first-row tile (ti = 0; those cover every row of the matrix); for the gemm
-// the X columns of a first-row tile and the P rows of a first-column tile. Every line is prefetched
-// once per launch, spread over many tiles and threads. Only matrices with small operands (pf_a set).
-template <int PHASE, int BN>
-__device__ __forceinline__ void prefetch_ahead(const TcBucket& B, const int4& a, int tid) {
-  if (B.pf_a == nullptr) return;
-  constexpr int kThreads = 256;
-  if (PHASE != kPhaseGemm) {
-    if (a.z != 0) return;
-    const char* base = B.pf_b + a.y * B.pf_b_stride;
-    const int r0 = a.w * BN, lines = (B.kdim * 2 + 127) / 128;
-    for (int t = tid; t < BN * lines; t += kThreads) {
-      const int r = r0 + t / lines;
-      if (r < B.m) ptx::prefetch_l2(base + (int64_t)r * B.pf_b_ld + (t % lines) * 128);
-    }
-  } else {
-    if (a.z == 0) {  // X rows 0..m-1, columns tj*BN.. (BN/64 lines of 128 bytes per row, inside the row)
-      const char* base = B.pf_b + a.y * B.pf_b_stride + (int64_t)a.w * BN * 2;
-      constexpr int lines = BN * 2 / 128;
-      for (int t = tid; t < B.m * lines; t += kThreads)
-        if (a.w * BN + (t % lines) * 64 < B.n)
-          ptx::prefetch_l2(base + (int64_t)(t / lines) * B.pf_b_ld + (t % lines) * 128);
-    }
-    if (a.w == 0) {  // P rows ti*128.., K = m
-      const char* base = B.pf_a + a.y * B.pf_a_stride;
-      const int r0 = a.z * kTcBM, lines = (B.m * 2 + 127) / 128;
-      for (int t = tid; t < kTcBM * lines; t += kThreads) {
-        const int r = r0 + t / lines;
-        if (r < B.m) ptx::prefetch_l2(base + (int64_t)r * B.pf_a_ld + (t % lines) * 128);
-      }
-    }
-  }
-}
-
 // First output column of a symmetric-product tile (bucket, slot, ti, tj):
 // the planner lists each row block's tiles from its diagonal block on.
 template <int BN>
@@ -328,10 +292,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
-      if (w + static_cast<int>(gridDim.x) < p.n_items) {  // while the MMAs of this tile still run
-        const int4 ahead = p.items[w + gridDim.x];
-        prefetch_ahead<PHASE, BN>(p.bk[ahead.x], ahead, threadIdx.x - 64);
-      }
       const int i0 = it.z * kTcBM + q * 32;
       const int jbase = (PHASE == kPhaseGemm ? it.w * BN : sym_col0<BN>(it)) + half * (BN / 2);
       const uint32_t tbase = tmem + acc * BN + half * (BN / 2) + ((uint32_t)(q * 32) << 16);
