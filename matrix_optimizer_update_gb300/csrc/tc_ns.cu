@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         return w < static_cast<unsigned>(p.n_items) ? static_cast<int>(w) : -1;
       };
       uint32_t stage = 0, phase = 0, j = 0;
-      uint32_t issued[kTcStages];
-      for (int s = 0; s < kTcStages; ++s) issued[s] = 0;
+      uint32_t fills = 0;  // stages filled so far: fill f went to stage f % stages
       int w = claim(0);
       for (;;) {
         const uint32_t slot = j % kSchedDepth;
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           } else {  // rows of the tile's columns; rows past the matrix's edge are zero-filled
             ptx::tma_load_3d(sB + stage * kStageB, &B.tmB, &sh->full[stage], k0, sym_col0<BN>(it), it.y);
           }
-          ++issued[stage];
+          ++fills;
           if (++stage == kTcStages) {
             stage = 0;
             phase ^= 1u;
@@ -213,10 +212,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
         w = next;
       }
       // Every issued copy must land before the CTA may exit (matters only after an abort).
-      for (int s = 0; s < kTcStages; ++s) {
-        if (issued[s]) {
+      for (uint32_t s = 0; s < kTcStages; ++s) {
+        if (fills > s) {
+          const uint32_t n = (fills - 1u - s) / kTcStages + 1u;  // fills of stage s
           int zero = 0;
-          ptx::mbar_wait(&sh->full[s], (issued[s] - 1u) & 1u, &zero, p.status, p.timeout_ns);
+          ptx::mbar_wait(&sh->full[s], (n - 1u) & 1u, &zero, p.status, p.timeout_ns);
         }
       }
     }

@@ -101,8 +101,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       // ------------------------------------------------------------ TMA producer (both CTAs)
       const uint32_t lead_full = ptx::mapa_shared(ptx::smem_u32(&sh->full[0]), 0);
       uint32_t stage = 0, phase = 0;
-      uint32_t issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      uint32_t fills = 0;  // stages filled so far: fill f went to stage f % stages
       for (int w = pair; w < p.n_items; w += npairs) {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
@@ -125,7 +124,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
           } else {  // symmetric products list a row pair's tiles from its diagonal block on
             ptx::tma_load_3d_pair(sB + stage * kHalfB, &B.tmB, fb, k0, (it.z + it.w) * kPairBN + rank * 128, it.y);
           }
-          ++issued[stage];
+          ++fills;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -136,10 +135,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       // The leader's full barriers count both CTAs' bytes: once their last
       // phases complete, no load of either CTA is still in flight.
       if (leader) {
-        for (int s = 0; s < kStages; ++s) {
-          if (issued[s]) {
+        for (uint32_t s = 0; s < kStages; ++s) {
+          if (fills > s) {
+            const uint32_t n = (fills - 1u - s) / kStages + 1u;  // fills of stage s
             int zero = 0;
-            ptx::mbar_wait_cluster(&sh->full[s], (issued[s] - 1u) & 1u, &zero, p.status, p.timeout_ns);
+            ptx::mbar_wait_cluster(&sh->full[s], (n - 1u) & 1u, &zero, p.status, p.timeout_ns);
           }
         }
       }
