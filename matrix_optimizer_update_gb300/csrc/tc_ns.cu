@@ -80,22 +80,20 @@ struct TcShared {
   uint64_t mma_done;
   uint64_t sched_full[kSchedDepth];   // item published (1 arrival: the TMA thread)
   uint64_t sched_empty[kSchedDepth];  // item read by the MMA thread and every epilogue warp
-  int4 ring[kSchedDepth];             // the item (bucket, slot, ti, tj); bucket -1 = no more tiles
+  int ring[kSchedDepth];              // item index, -1 = no more tiles
   uint32_t tmem_base;
   int abort_flag;
 };
 
 static_assert(sizeof(TcShared<6>) <= 1024, "barriers must fit their 1 KB");
 
-// Consumer side of the item ring: the j-th item of this CTA (false when the CTA gives up). The
-// ring carries the item itself, so no consumer waits on a global load at a tile's start.
+// Consumer side of the item ring: the j-th item of this CTA (false when the CTA gives up).
 template <int STAGES>
-__device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int4& it, volatile int* abortf,
+__device__ __forceinline__ bool ring_take(TcShared<STAGES>* sh, uint32_t j, int& w, volatile int* abortf,
                                           const TcParams& p) {
   const uint32_t slot = j % kSchedDepth;
   if (!ptx::mbar_wait(&sh->sched_full[slot], (j / kSchedDepth) & 1u, abortf, p.status, p.timeout_ns)) return false;
-  const volatile int4* r = &sh->ring[slot];
-  it = make_int4(r->x, r->y, r->z, r->w);
+  w = *reinterpret_cast<volatile int*>(&sh->ring[slot]);
   ptx::mbar_arrive(&sh->sched_empty[slot]);
   return true;
 }
@@ -163,38 +161,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       // Also the tile scheduler: with p.sched, tiles are claimed from the launch's counter in
-      // list order (largest cost first) as this CTA gets to them; without it, CTA b takes items
-      // b, b + grid, b + 2*grid, ... Claims run two tiles ahead and the next item is read from
-      // the list one tile ahead, so that neither the atomic nor the load delays a tile's first
-      // copies. Each item goes into the ring for the MMA thread and the epilogue warps; an item
-      // with bucket -1 ends the list.
-      uint32_t nclaims = 0;
-      auto claim = [&]() -> int {
+      // list order (largest cost first) as this CTA gets to them, one claim ahead of the loads;
+      // without it, CTA b takes items b, b + grid, b + 2*grid, ... Either way each claimed item
+      // goes into the ring for the MMA thread and the epilogue warps; -1 ends the list.
+      auto claim = [&](uint32_t j) -> int {
         if (p.sched == nullptr) {
-          const int64_t w = blockIdx.x + static_cast<int64_t>(nclaims++) * gridDim.x;
+          const int64_t w = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
           return w < p.n_items ? static_cast<int>(w) : -1;
         }
         const unsigned w = atomicAdd(p.sched, 1u);
         return w < static_cast<unsigned>(p.n_items) ? static_cast<int>(w) : -1;
       };
-      const int4 kEnd = make_int4(-1, 0, 0, 0);
       uint32_t stage = 0, phase = 0, j = 0;
       uint32_t fills = 0;  // stages filled so far: fill f went to stage f % stages
-      const int w0 = claim();
-      int4 it_cur = w0 >= 0 ? p.items[w0] : kEnd;
-      int w_next = w0 >= 0 ? claim() : -1;
+      int w = claim(0);
       for (;;) {
         const uint32_t slot = j % kSchedDepth;
         if (!ptx::mbar_wait(&sh->sched_empty[slot], ((j / kSchedDepth) & 1u) ^ 1u, abortf, p.status, p.timeout_ns))
           break;
-        sh->ring[slot] = it_cur;
+        sh->ring[slot] = w;
         ptx::mbar_arrive(&sh->sched_full[slot]);
         ++j;
-        if (it_cur.x < 0) break;
-        // the next tile's item (its load) and the claim after it: both in flight under this tile's loads
-        const int4 it_next = w_next >= 0 ? p.items[w_next] : kEnd;
-        const int w_after = w_next >= 0 ? claim() : -1;
-        const int4 it = it_cur;
+        if (w < 0) break;
+        const int next = claim(j);  // its latency hides under this tile's loads
+        const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         const bool a_in_b = a_rows_in_b(B, it);
@@ -219,8 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
           }
         }
         if (!ok) break;
-        it_cur = it_next;
-        w_next = w_after;
+        w = next;
       }
       // Every issued copy must land before the CTA may exit (matters only after an abort).
       for (uint32_t s = 0; s < kTcStages; ++s) {
@@ -238,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
       constexpr uint32_t idesc_half = ptx::idesc_bf16(kTcBM, BN / 2, PHASE == kPhaseGemm);
       uint32_t stage = 0, phase = 0, local = 0;
       bool ok = true;
-      for (int4 it; ok && ring_take(sh, local, it, abortf, p) && it.x >= 0; ++local) {
+      for (int w; ok && ring_take(sh, local, w, abortf, p) && w >= 0; ++local) {
+        const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         const uint32_t acc = local & 1u;
@@ -295,14 +285,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
     uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
     uint32_t local = 0, nbox = 0;
     for (;; ++local) {
-      int4 it = make_int4(-2, 0, 0, 0);  // bucket -2: the CTA gave up
-      if (lane == 0 && !ring_take(sh, local, it, abortf, p)) it.x = -2;
-      it.x = __shfl_sync(0xffffffffu, it.x, 0);
-      it.y = __shfl_sync(0xffffffffu, it.y, 0);
-      it.z = __shfl_sync(0xffffffffu, it.z, 0);
-      it.w = __shfl_sync(0xffffffffu, it.w, 0);
-      if (it.x < 0) break;
+      int w = -2;  // -2: the CTA gave up
+      if (lane == 0 && !ring_take(sh, local, w, abortf, p)) w = -2;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) break;
       const uint32_t acc = local & 1u;
+      const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
       const int i0 = it.z * kTcBM + q * 32;
       const int jbase = (PHASE == kPhaseGemm ? it.w * BN : sym_col0<BN>(it)) + half * (BN / 2);
