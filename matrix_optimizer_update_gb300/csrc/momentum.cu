@@ -90,8 +90,12 @@ __device__ __forceinline__ double block_sum_d(double v, double* red) {
   return t;
 }
 
+// Resident CTAs per SM the momentum kernel is compiled for: more warps keep its loads in flight when
+// the SM clock drops (as it does under the power limit right after the tensor-core phases).
+constexpr int kMomentumCtasPerSm = 4;
+
 template <bool GB, bool XB>
-__global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(kStreamThreads, kMomentumCtasPerSm) momentum_kernel(const __grid_constant__ StreamParams p) {
   __shared__ float tileU[kTileR][kTileC + 1];
   const float mu = p.mu;
   const bool nest = p.nesterov != 0;
@@ -110,31 +114,36 @@ __global__ void __launch_bounds__(kStreamThreads) momentum_kernel(const __grid_c
       const int64_t e0 = local * kFlatUnit;
       const int64_t e1 = min(e0 + kFlatUnit, total);
       constexpr int kV = kFlatUnit / (8 * kStreamThreads);  // 8-element vectors per thread
+      constexpr int kH = 2;                                   // of which in flight together
       if (e0 + kFlatUnit <= total) {
-        // full unit: every load of the thread is issued before any store
-        float g[kV][8];
-        float4 m0[kV], m1[kV];
+        // full unit, kH vectors at a time: every load of a group is issued before its stores, and
+        // the registers this takes leave room for 4 CTAs per SM
 #pragma unroll
-        for (int k = 0; k < kV; ++k) {
-          const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
-          load8_grad<GB>(G, e, g[k]);
-          m0[k] = __ldcs(reinterpret_cast<const float4*>(M + e));
-          m1[k] = __ldcs(reinterpret_cast<const float4*>(M + e + 4));
-        }
+        for (int h = 0; h < kV; h += kH) {
+          float g[kH][8];
+          float4 m0[kH], m1[kH];
 #pragma unroll
-        for (int k = 0; k < kV; ++k) {
-          const int64_t e = e0 + (int64_t)(threadIdx.x + k * kStreamThreads) * 8;
-          float mv[8] = {m0[k].x, m0[k].y, m0[k].z, m0[k].w, m1[k].x, m1[k].y, m1[k].z, m1[k].w};
-          float uu[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            mv[q] = fmaf(mu, mv[q], g[k][q]);
-            uu[q] = nest ? fmaf(mu, mv[q], g[k][q]) : mv[q];
-            ss = fmaf(uu[q], uu[q], ss);
+          for (int k = 0; k < kH; ++k) {
+            const int64_t e = e0 + (int64_t)(threadIdx.x + (h + k) * kStreamThreads) * 8;
+            load8_grad<GB>(G, e, g[k]);
+            m0[k] = __ldcs(reinterpret_cast<const float4*>(M + e));
+            m1[k] = __ldcs(reinterpret_cast<const float4*>(M + e + 4));
           }
-          __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
-          __stcs(reinterpret_cast<float4*>(M + e + 4), make_float4(mv[4], mv[5], mv[6], mv[7]));
-          store8_x<XB>(X, e, uu);
+#pragma unroll
+          for (int k = 0; k < kH; ++k) {
+            const int64_t e = e0 + (int64_t)(threadIdx.x + (h + k) * kStreamThreads) * 8;
+            float mv[8] = {m0[k].x, m0[k].y, m0[k].z, m0[k].w, m1[k].x, m1[k].y, m1[k].z, m1[k].w};
+            float uu[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              mv[q] = fmaf(mu, mv[q], g[k][q]);
+              uu[q] = nest ? fmaf(mu, mv[q], g[k][q]) : mv[q];
+              ss = fmaf(uu[q], uu[q], ss);
+            }
+            __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
+            __stcs(reinterpret_cast<float4*>(M + e + 4), make_float4(mv[4], mv[5], mv[6], mv[7]));
+            store8_x<XB>(X, e, uu);
+          }
         }
       } else {
         for (int64_t q = e0 + threadIdx.x; q < e1; q += kStreamThreads) {

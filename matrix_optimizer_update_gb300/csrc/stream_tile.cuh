@@ -46,45 +46,50 @@ __device__ __forceinline__ void store1_x(void* dst, int64_t e, float v) {
 // Rows r0.. (64) and columns c0.. (128) of the stored rows x cols matrix:
 // update M, leave U in `tile` (zero outside the matrix) and return this
 // thread's sum of U^2. Each thread takes 4 consecutive columns of 8 rows;
-// with vec (cols % 4 == 0 and aligned G, M) a full tile issues all its loads
-// before any store. Ends before the __syncthreads that publishes `tile`.
+// with vec (cols % 4 == 0 and aligned G, M) a full tile issues the loads of
+// half its rows before their stores, then the other half's. Ends before the
+// __syncthreads that publishes `tile`.
 template <bool GB>
 __device__ __forceinline__ float tile_update(const void* G, float* M, int rows, int cols, bool vec, int r0, int c0,
                                              float mu, bool nest, Tile& tile) {
   float ss = 0.f;
   const int cc = (threadIdx.x & 31) * 4;
   if (vec && r0 + kTileR <= rows && c0 + kTileC <= cols) {
-    constexpr int kP = kTileR / 8;
-    float g[kP][4];
-    float4 m4[kP];
+    constexpr int kP = kTileR / 8;  // passes of 8 rows
+    constexpr int kH = kP / 2;      // passes whose loads are in flight together
 #pragma unroll
-    for (int pass = 0; pass < kP; ++pass) {
-      const int rr = pass * 8 + (threadIdx.x >> 5);
-      const int64_t e = (int64_t)(r0 + rr) * cols + c0 + cc;
-      if (GB) {
-        const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-        g[pass][0] = f0.x, g[pass][1] = f0.y, g[pass][2] = f1.x, g[pass][3] = f1.y;
-      } else {
-        const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e));
-        g[pass][0] = f.x, g[pass][1] = f.y, g[pass][2] = f.z, g[pass][3] = f.w;
+    for (int h = 0; h < kP; h += kH) {
+      float g[kH][4];
+      float4 m4[kH];
+#pragma unroll
+      for (int k = 0; k < kH; ++k) {
+        const int rr = (h + k) * 8 + (threadIdx.x >> 5);
+        const int64_t e = (int64_t)(r0 + rr) * cols + c0 + cc;
+        if (GB) {
+          const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const bf16*>(G) + e));
+          const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          const float2 f0 = __bfloat1622float2(hh[0]), f1 = __bfloat1622float2(hh[1]);
+          g[k][0] = f0.x, g[k][1] = f0.y, g[k][2] = f1.x, g[k][3] = f1.y;
+        } else {
+          const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(G) + e));
+          g[k][0] = f.x, g[k][1] = f.y, g[k][2] = f.z, g[k][3] = f.w;
+        }
+        m4[k] = __ldcs(reinterpret_cast<const float4*>(M + e));
       }
-      m4[pass] = __ldcs(reinterpret_cast<const float4*>(M + e));
-    }
 #pragma unroll
-    for (int pass = 0; pass < kP; ++pass) {
-      const int rr = pass * 8 + (threadIdx.x >> 5);
-      const int64_t e = (int64_t)(r0 + rr) * cols + c0 + cc;
-      float mv[4] = {m4[pass].x, m4[pass].y, m4[pass].z, m4[pass].w};
+      for (int k = 0; k < kH; ++k) {
+        const int rr = (h + k) * 8 + (threadIdx.x >> 5);
+        const int64_t e = (int64_t)(r0 + rr) * cols + c0 + cc;
+        float mv[4] = {m4[k].x, m4[k].y, m4[k].z, m4[k].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mv[q] = fmaf(mu, mv[q], g[pass][q]);
-        const float uu = nest ? fmaf(mu, mv[q], g[pass][q]) : mv[q];
-        ss = fmaf(uu, uu, ss);
-        tile[rr][cc + q] = uu;
+        for (int q = 0; q < 4; ++q) {
+          mv[q] = fmaf(mu, mv[q], g[k][q]);
+          const float uu = nest ? fmaf(mu, mv[q], g[k][q]) : mv[q];
+          ss = fmaf(uu, uu, ss);
+          tile[rr][cc + q] = uu;
+        }
+        __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
       }
-      __stcs(reinterpret_cast<float4*>(M + e), make_float4(mv[0], mv[1], mv[2], mv[3]));
     }
   } else {
     for (int pass = 0; pass < kTileR / 8; ++pass) {
