@@ -486,10 +486,19 @@ def tuned_buckets(plan):
     return [{k: b[k] for k in ("m", "n", "pair", "bn_sym", "bn_gemm", "tune_cost")} for b in plan.describe()["buckets"]]
 
 
+def tile_kinds(plan):
+    """Matrices per tile kind of a plan: two-SM 256 x 256 pairs or one-SM 128-row tiles."""
+    out = {}
+    for b in plan.describe()["buckets"]:
+        k = "two-SM 256x256" if b["pair"] else f"one-SM 128x{b['bn_sym']}/128x{b['bn_gemm']}"
+        out[k] = out.get(k, 0) + b["count"]
+    return out
+
+
 def plan_flags(args):
     from matrix_optimizer_update_gb300 import dmuon as dm
 
-    return ((dm.FLAG_PAIR_TILES if args.pair else 0) | (dm.FLAG_STATIC_TILES if args.static_tiles else 0)
+    return ((dm.FLAG_ONE_SM_TILES if args.one_sm else 0) | (dm.FLAG_STATIC_TILES if args.static_tiles else 0)
             | (dm.FLAG_TUNE if args.tune else 0))
 
 
@@ -527,6 +536,7 @@ def run_ours(args):
     desc = plan.describe()
     launches_per_step = len(desc["launches"])
     headline_buckets = tuned_buckets(plan) if args.tune else None
+    tiles = tile_kinds(plan)
     Wp, Gp, Mp = ms.ptrs(ms.W), ms.ptrs(ms.G), ms.ptrs(ms.M)
     sh = stream.cuda_stream
 
@@ -761,7 +771,7 @@ def run_ours(args):
         "config": {"workload": w.name, "matrices": tot["matrices"], "params": tot["params"],
                    "ns_steps": w.ns_steps, "ns_flops_per_step": tot["ns_flops"],
                    "storage": {"param": w.param_dtype, "grad": w.grad_dtype, "momentum": "f32"},
-                   "parallelism": f"replicas{world}", "tiles": "two-SM 256x256" if args.pair else "one-SM 128x256",
+                   "parallelism": f"replicas{world}", "tiles": tiles,
                    "tile_schedule": "dealt round-robin" if args.static_tiles else "claimed from a counter",
                    "tuned": bool(args.tune),
                    **({"tuned_buckets": headline_buckets} if args.tune else {}),
@@ -799,7 +809,8 @@ def main(argv=None):
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other matrix sets")
     ap.add_argument("--per-workload-steps", type=int, default=5, help="timed steps per other matrix set")
-    ap.add_argument("--pair", action="store_true", help="256 x 256 tiles on CTA pairs (two-SM UMMA)")
+    ap.add_argument("--one-sm", action="store_true",
+                    help="one-SM tiles everywhere instead of 256 x 256 tiles on CTA pairs where they fit")
     ap.add_argument("--static-tiles", action="store_true", help="deal tiles round-robin instead of claiming them")
     ap.add_argument("--tune", action="store_true", help="choose tile configurations by timing them at bind")
     ap.add_argument("--adamw", action="store_true",

@@ -92,12 +92,13 @@ typedef struct {
                                           Space Recurrence"). Fewer flops when the
                                           matrix is wide (>= 26% fewer at 2:1);
                                           others keep the standard form.          */
-#define DMUON_FLAG_PAIR_TILES 0x8u    /* buckets whose short side is a multiple
+#define DMUON_FLAG_PAIR_TILES 0x8u    /* the default, accepted for callers that set
+                                          it: buckets whose short side is a multiple
                                           of 256 and whose products run 256 wide use
-                                          256 x 256 tiles on pairs of SMs
-                                          (two-SM UMMA, thread-block clusters of
-                                          2). bf16 only. Test hook: with the
-                                          environment variable
+                                          256 x 256 tiles on pairs of SMs (two-SM
+                                          UMMA, thread-block clusters of 2; bf16
+                                          only), other buckets one-SM tiles. Test
+                                          hook: with the environment variable
                                           DMUON_TEST_FORCE_PAIRS=1, every bucket
                                           with a short side >= 256 gets pairs (as
                                           DMUON_FLAG_TUNE may choose).           */
@@ -112,12 +113,13 @@ typedef struct {
                                           no X_k tile: the same polynomial, one
                                           bf16 rounding of a + B_ii instead of
                                           an fp32 a*X term.                      */
-#define DMUON_FLAG_STATIC_TILES 0x20u  /* one-SM tensor-core launches deal the cost-ordered
-                                          tile list round-robin (CTA b takes tiles b,
-                                          b + grid, ...) instead of letting each CTA
-                                          claim the next tile from the launch's counter
-                                          as it becomes free. Same results bit for bit;
-                                          kept to compare the two schedules.       */
+#define DMUON_FLAG_STATIC_TILES 0x20u  /* tensor-core launches deal the cost-ordered
+                                          tile list round-robin (CTA b, or CTA pair b,
+                                          takes tiles b, b + grid, ...) instead of
+                                          letting each CTA (pair) claim the next tile
+                                          from the launch's counter as it becomes free.
+                                          Same results bit for bit; kept to compare the
+                                          two schedules.                           */
 #define DMUON_FLAG_DEBUG_CHECKS 0x40u /* debugging aid: after every launch of a step
                                           the host waits for it, copies back the
                                           operands of a few sampled output elements
@@ -133,6 +135,10 @@ typedef struct {
                                           DMUON_TEST_SKIP_LAUNCH=<i>, launch i of
                                           each step is left out, so its outputs are
                                           stale and the checks must report them.  */
+#define DMUON_FLAG_ONE_SM_TILES 0x80u /* every bucket uses one-SM tiles (128 rows,
+                                          128 or 256 columns): no CTA pairs. Not
+                                          together with DMUON_FLAG_PAIR_TILES or
+                                          DMUON_FLAG_TUNE.                        */
 #define DMUON_FLAG_TUNE 0x4u           /* at bind, time three tile configurations per
                                           bucket on the bound workspace (one-SM
                                           128 x 128 and 128 x 256 tiles, two-SM
@@ -327,8 +333,8 @@ dmuon_status dmuon_plan_costs(dmuon_plan_t plan, double* per_matrix_ms, int32_t 
  * records of launch `launch` (its index in dmuon_plan_describe's launch list)
  * of the last recorded step to out[2*i] (start) and out[2*i+1] (end) for CTA
  * i < min(cap, *n_ctas), host memory, synchronising stream; *n_ctas receives
- * the launch's CTA count (0 for launches that keep no records: streaming
- * kernels, fp32 mode and CTA pairs).
+ * the launch's CTA count (both CTAs of each pair for two-SM tiles; 0 for
+ * launches that keep no records: streaming kernels and fp32 mode).
  */
 dmuon_status dmuon_profile_cta_times(dmuon_plan_t plan, int32_t enable);
 dmuon_status dmuon_read_cta_times(dmuon_plan_t plan, int32_t launch, uint64_t* out, int32_t cap, int32_t* n_ctas,

@@ -344,12 +344,12 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn_gemm(order[b].second) : kSimtBN;
-    // two-SM 256 x 256 tiles where both dimensions fill them: no 256-row tile is left half empty
-    // (tuning may still choose them for other short sides >= 256, and so does the test hook)
-    const bool pair_flag = P.tc && (P.flags & DMUON_FLAG_PAIR_TILES);
-    const bool forced = pair_flag && order[b].first >= 256 && test_hook_env("DMUON_TEST_FORCE_PAIRS");
+    // two-SM 256 x 256 tiles (the default) where both dimensions fill them: no 256-row tile is left
+    // half empty (tuning may still choose them for other short sides >= 256, and so does the test hook)
+    const bool pairs_on = P.tc && !(P.flags & DMUON_FLAG_ONE_SM_TILES);
+    const bool forced = pairs_on && order[b].first >= 256 && test_hook_env("DMUON_TEST_FORCE_PAIRS");
     if (forced) P.buckets[b].bn_sym = P.buckets[b].bn_gemm = 256;
-    P.buckets[b].pair = forced || (pair_flag && order[b].first % 256 == 0 && P.buckets[b].bn_sym == 256 &&
+    P.buckets[b].pair = forced || (pairs_on && order[b].first % 256 == 0 && P.buckets[b].bn_sym == 256 &&
                                    P.buckets[b].bn_gemm == 256);
   }
 
@@ -852,9 +852,8 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
         tp.status = P.sp.status;
         tp.param_bf16 = P.sp.param_bf16;
         tp.timeout_ns = 2000000000LL;
-        tp.sched = (P.flags & DMUON_FLAG_STATIC_TILES) || T.pair
-                       ? nullptr
-                       : reinterpret_cast<unsigned*>(P.ws + P.off_probe_sched);
+        tp.sched = (P.flags & DMUON_FLAG_STATIC_TILES) ? nullptr
+                                                        : reinterpret_cast<unsigned*>(P.ws + P.off_probe_sched);
         const int grid = std::max(1, std::min(n, slots));
         auto launch = [&]() {
           return T.pair ? launch_tc_pair(phase, tp, grid, s) : launch_tc(phase, T.bn_sym, tp, grid, s);
@@ -1241,8 +1240,10 @@ dmuon_status dmuon_plan(const dmuon_shape* shapes, int32_t n_mats, int32_t ns_st
   if (ns_steps < 0 || ns_steps > 16) return fail(DMUON_ERR_INVALID_ARG, "ns_steps %d outside 0..16", ns_steps);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (flags & ~(DMUON_FLAG_CAPTURE_UPDATE | DMUON_FLAG_GRAM_NS | DMUON_FLAG_TUNE | DMUON_FLAG_PAIR_TILES |
-                DMUON_FLAG_EPILOGUE_AX | DMUON_FLAG_STATIC_TILES | DMUON_FLAG_DEBUG_CHECKS))
+                DMUON_FLAG_EPILOGUE_AX | DMUON_FLAG_STATIC_TILES | DMUON_FLAG_DEBUG_CHECKS | DMUON_FLAG_ONE_SM_TILES))
     return fail(DMUON_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags);
+  if ((flags & DMUON_FLAG_ONE_SM_TILES) && (flags & (DMUON_FLAG_PAIR_TILES | DMUON_FLAG_TUNE)))
+    return fail(DMUON_ERR_INVALID_ARG, "DMUON_FLAG_ONE_SM_TILES excludes DMUON_FLAG_PAIR_TILES and DMUON_FLAG_TUNE");
   for (int32_t d : {dtypes.param, dtypes.grad, dtypes.compute})
     if (d != DMUON_F32 && d != DMUON_BF16) return fail(DMUON_ERR_UNSUPPORTED, "unknown dtype %d", d);
   if (dtypes.momentum != DMUON_F32) return fail(DMUON_ERR_UNSUPPORTED, "momentum must be DMUON_F32");
@@ -1432,7 +1433,7 @@ dmuon_status dmuon_plan_bind(dmuon_plan_t P, void* d_workspace, size_t bytes, vo
       tp.param_bf16 = sp.param_bf16;
       tp.timeout_ns = 2000000000LL;
       const size_t li = static_cast<size_t>(&L - P->launches.data());
-      tp.sched = (L.pair || (P->flags & DMUON_FLAG_STATIC_TILES))
+      tp.sched = (P->flags & DMUON_FLAG_STATIC_TILES)
                      ? nullptr
                      : reinterpret_cast<unsigned*>(ws + P->off_sched + kSchedBytes * static_cast<int64_t>(li));
       L.grid = L.pair ? std::max(1, std::min(lr.count, P->num_sms / 2)) : std::max(1, std::min(lr.count, P->num_sms));
@@ -1843,11 +1844,11 @@ dmuon_status dmuon_read_cta_times(dmuon_plan_t P, int32_t launch, uint64_t* out,
   const Launch& L = P->launches[launch];
   const bool tc_kind = L.kind == DMUON_KIND_GRAM || L.kind == DMUON_KIND_POLY || L.kind == DMUON_KIND_GEMM ||
                        L.kind == DMUON_KIND_SYMM;
-  if (!P->tc || !tc_kind || L.pair) {
+  if (!P->tc || !tc_kind) {
     *n_ctas = 0;
     return DMUON_OK;
   }
-  const int n = std::min<int>(L.grid, kMaxCtaRecords);
+  const int n = std::min<int>(L.pair ? 2 * L.grid : L.grid, kMaxCtaRecords);  // a pair launch's grid counts pairs
   *n_ctas = n;
   if (out == nullptr || cap <= 0) return DMUON_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -101,9 +101,9 @@ struct TcParams {
   unsigned* status;
   int32_t param_bf16;
   int64_t timeout_ns;
-  // Dynamic tile claiming (one-SM kernel): [0] counts claimed items, [1] CTAs that finished;
-  // both zero before the launch, and the last CTA leaves them zero. nullptr = CTA b takes items
-  // b, b + grid, ... (the two-SM kernel always does).
+  // Dynamic tile claiming: [0] counts claimed items, [1] CTAs that finished; both zero before
+  // the launch, and the last CTA leaves them zero. nullptr = CTA b (CTA pair b of the two-SM
+  // kernel) takes items b, b + grid, ...
   unsigned* sched;
   unsigned long long* cta_times;  // profiling: start and end (global timer, ns) per CTA, or nullptr
 };

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_kernel(const __grid_const
 
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (p.cta_times != nullptr) {  // profiling: this CTA's start and end on the global timer
+    if (p.cta_times != nullptr && blockIdx.x < kMaxCtaRecords) {  // profiling: this CTA's start and end
       p.cta_times[2 * blockIdx.x] = t_start;
       p.cta_times[2 * blockIdx.x + 1] = ptx::globaltimer();
     }

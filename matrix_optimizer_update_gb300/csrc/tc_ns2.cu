@@ -23,6 +23,11 @@
 //  - cluster barriers after set-up and before TMEM is released, so that no
 //    CTA signals an uninitialised barrier or leaves while the leader's MMAs
 //    still read its shared memory or write its TMEM.
+// Tiles: the leader's TMA thread claims them from the launch's counter (or
+// deals them, pair b taking items b, b + pairs, ...) and writes each item into
+// a ring in both CTAs (sched_full in each CTA, one arrival from the leader);
+// the leader's MMA thread, the peer's TMA thread and the epilogue warps of
+// both take it from their own ring and arrive on the leader's sched_empty.
 // All mbarrier waits are bounded as in tc_ns.cu.
 #include <cuda_bf16.h>
 
@@ -44,17 +49,35 @@ constexpr uint32_t kTmemCols = 2 * kPairBN;    // two 128 x 256 fp32 accumulator
 constexpr int kEpiWarps = 8;
 constexpr int kEpiChunks = kPairBN / 2 / 32;
 
+constexpr int kSchedDepth = 8;                     // items in flight between the claim and the epilogue
+constexpr uint32_t kSchedConsumers = 2 + 2 * kEpiWarps;  // leader's MMA thread, peer's TMA thread, epilogue warps
+
 struct PairShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
+  uint64_t sched_full[kSchedDepth];   // this CTA's ring slot written (1 arrival: the leader's TMA thread)
+  uint64_t sched_empty[kSchedDepth];  // used in the leader: the slot read by every consumer of both CTAs
+  int ring[kSchedDepth];              // item index, -1 = no more tiles
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(PairShared) <= 1024, "barriers must fit their 1 KB");
 using epi::kStageBox;
+
+// Consumer side of the item ring: the j-th item of this pair (false when the CTA gives up).
+// lead_empty: cluster address of the leader's sched_empty[0].
+__device__ __forceinline__ bool pair_take(PairShared* sh, uint32_t j, int& w, uint32_t lead_empty,
+                                          volatile int* abortf, const TcParams& p) {
+  const uint32_t slot = j % kSchedDepth;
+  if (!ptx::mbar_wait_cluster(&sh->sched_full[slot], (j / kSchedDepth) & 1u, abortf, p.status, p.timeout_ns))
+    return false;
+  w = *reinterpret_cast<volatile int*>(&sh->ring[slot]);
+  ptx::mbar_arrive_cluster(lead_empty + slot * static_cast<uint32_t>(sizeof(uint64_t)));
+  return true;
+}
 
 template <int PHASE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_constant__ TcParams p) {
@@ -81,6 +104,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       ptx::mbar_init(&sh->tempty[a], 2 * kEpiWarps);
     }
     ptx::mbar_init(&sh->mma_done, 1);
+    for (int k = 0; k < kSchedDepth; ++k) {
+      ptx::mbar_init(&sh->sched_full[k], 1);
+      ptx::mbar_init(&sh->sched_empty[k], kSchedConsumers);
+    }
     sh->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -95,6 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
   const uint32_t tmem = sh->tmem_base;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int npairs = static_cast<int>(gridDim.x >> 1);
+  const uint32_t lead_empty = ptx::mapa_shared(ptx::smem_u32(&sh->sched_empty[0]), 0);
+  const uint64_t t_start = ptx::globaltimer();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -102,18 +131,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       const uint32_t lead_full = ptx::mapa_shared(ptx::smem_u32(&sh->full[0]), 0);
       uint32_t stage = 0, phase = 0;
       uint32_t fills = 0;  // stages filled so far: fill f went to stage f % stages
-      for (int w = pair; w < p.n_items; w += npairs) {
+      auto load_tile = [&](int w) -> bool {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
         // a diagonal pair tile of a matrix with itself: each CTA's A rows are its B rows
         const bool a_in_b = PHASE != kPhaseGemm && B.same_ab && it.w == 0;
-        bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait_cluster(&sh->empty[stage], phase ^ 1u, abortf, p.status, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
+          if (!ptx::mbar_wait_cluster(&sh->empty[stage], phase ^ 1u, abortf, p.status, p.timeout_ns)) return false;
           if (leader) ptx::mbar_arrive_expect_tx(&sh->full[stage], 2 * ((a_in_b ? 0u : kHalfA) + kHalfB));
           const uint32_t fb = lead_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
           const int k0 = kb * kTcBK;
@@ -130,7 +155,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
             phase ^= 1u;
           }
         }
-        if (!ok) break;
+        return true;
+      };
+      if (leader) {
+        // Also the pair's tile scheduler: with p.sched, tiles are claimed from the launch's counter in
+        // list order as the pair gets to them, one claim ahead of the loads; without it, pair b takes
+        // items b, b + pairs, ... Each item goes into both CTAs' rings; -1 ends the list.
+        const uint32_t peer_ring = ptx::mapa_shared(ptx::smem_u32(&sh->ring[0]), 1);
+        const uint32_t peer_full = ptx::mapa_shared(ptx::smem_u32(&sh->sched_full[0]), 1);
+        auto claim = [&](uint32_t j) -> int {
+          if (p.sched == nullptr) {
+            const int64_t w = pair + static_cast<int64_t>(j) * npairs;
+            return w < p.n_items ? static_cast<int>(w) : -1;
+          }
+          const unsigned w = atomicAdd(p.sched, 1u);
+          return w < static_cast<unsigned>(p.n_items) ? static_cast<int>(w) : -1;
+        };
+        int w = claim(0);
+        for (uint32_t j = 0;; ++j) {
+          const uint32_t slot = j % kSchedDepth;
+          if (!ptx::mbar_wait_cluster(&sh->sched_empty[slot], ((j / kSchedDepth) & 1u) ^ 1u, abortf, p.status,
+                                      p.timeout_ns))
+            break;
+          sh->ring[slot] = w;
+          ptx::st_shared_cluster_s32(peer_ring + slot * 4u, w);
+          ptx::mbar_arrive(&sh->sched_full[slot]);
+          ptx::mbar_arrive_cluster(peer_full + slot * static_cast<uint32_t>(sizeof(uint64_t)));  // orders the store
+          if (w < 0) break;
+          const int next = claim(j + 1);  // its latency hides under this tile's loads
+          if (!load_tile(w)) break;
+          w = next;
+        }
+      } else {
+        for (uint32_t j = 0;; ++j) {
+          int w;
+          if (!pair_take(sh, j, w, lead_empty, abortf, p) || w < 0) break;
+          if (!load_tile(w)) break;
+        }
       }
       // The leader's full barriers count both CTAs' bytes: once their last
       // phases complete, no load of either CTA is still in flight.
@@ -150,7 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
       constexpr uint32_t idesc = ptx::idesc_bf16(kPairBM, kPairBN, PHASE == kPhaseGemm);
       uint32_t stage = 0, phase = 0, local = 0;
       bool ok = true;
-      for (int w = pair; w < p.n_items && ok; w += npairs, ++local) {
+      for (int w; ok && pair_take(sh, local, w, lead_empty, abortf, p) && w >= 0; ++local) {
         const int4 it = p.items[w];
         const TcBucket& B = p.bk[it.x];
         const int nk = (B.kdim + kTcBK - 1) / kTcBK;
@@ -195,7 +256,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
     const uint32_t lead_tempty = ptx::mapa_shared(ptx::smem_u32(&sh->tempty[0]), 0);
     uint8_t* stg = stg_all + (warp - 2) * (2 * kStageBox);
     uint32_t local = 0, nbox = 0;
-    for (int w = pair; w < p.n_items; w += npairs, ++local) {
+    for (;; ++local) {
+      int w = -2;  // -2: the CTA gave up
+      if (lane == 0 && !pair_take(sh, local, w, lead_empty, abortf, p)) w = -2;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) break;
       const uint32_t acc = local & 1u;
       const int4 it = p.items[w];
       const TcBucket& B = p.bk[it.x];
@@ -215,6 +280,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ns_pair_kernel(const __grid_
   }
 
   __syncthreads();
+  if (threadIdx.x == 0) {
+    if (p.cta_times != nullptr && blockIdx.x < kMaxCtaRecords) {  // profiling: this CTA's start and end
+      p.cta_times[2 * blockIdx.x] = t_start;
+      p.cta_times[2 * blockIdx.x + 1] = ptx::globaltimer();
+    }
+    if (p.sched != nullptr) {
+      // Every claim of a leader precedes its arrival here; the last CTA to arrive leaves both words
+      // at zero for the next launch that uses them.
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        p.sched[0] = 0u;
+        p.sched[1] = 0u;
+      }
+    }
+  }
   ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();

@@ -37,6 +37,7 @@ FLAG_PAIR_TILES = 0x8
 FLAG_EPILOGUE_AX = 0x10
 FLAG_STATIC_TILES = 0x20
 FLAG_DEBUG_CHECKS = 0x40
+FLAG_ONE_SM_TILES = 0x80
 DEV_NONFINITE_NORM = 0x1
 DEV_WAIT_TIMEOUT = 0x2
 

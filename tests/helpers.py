@@ -61,7 +61,9 @@ class LibRun:
     """Flat device buffers for one batch plus a bound plan."""
 
     def __init__(self, shapes, *, param="bf16", grad="bf16", compute="bf16", ns_steps=5, coeffs=ref.DEFAULT_COEFFS,
-                 eps=1e-7, capture=True, device="cuda", gram_ns=False, pair=False, epilogue_ax=False, flags=0):
+                 eps=1e-7, capture=True, device="cuda", gram_ns=False, pair=None, epilogue_ax=False, flags=0):
+        # pair: None = the library's default (two-SM tiles where they fill the short side), True = the
+        # same asked for explicitly, False = one-SM tiles everywhere
         self.shapes = list(shapes)
         self.param, self.grad, self.compute = param, grad, compute
         self.offs, total = layout(self.shapes)
@@ -71,7 +73,8 @@ class LibRun:
         self.muon = dm.Muon.create(self.shapes, ns_steps=ns_steps, coeffs=coeffs, eps=eps, param=param, grad=grad,
                                    compute=compute, device=device,
                                    flags=(dm.FLAG_CAPTURE_UPDATE if capture else 0) | (dm.FLAG_GRAM_NS if gram_ns else 0)
-                                   | (dm.FLAG_PAIR_TILES if pair else 0) | (dm.FLAG_EPILOGUE_AX if epilogue_ax else 0)
+                                   | {None: 0, True: dm.FLAG_PAIR_TILES, False: dm.FLAG_ONE_SM_TILES}[pair]
+                                   | (dm.FLAG_EPILOGUE_AX if epilogue_ax else 0)
                                    | flags)
         self.capture = capture
 

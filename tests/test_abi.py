@@ -51,8 +51,12 @@ def test_invalid_arguments_are_rejected_on_the_host():
         dm.dmuon_plan([(4, 4)], 3, eps=-1.0)
     assert e.value.status == dm.ERR_INVALID_ARG
     with pytest.raises(dm.DmuonError) as e:
-        dm.dmuon_plan([(4, 4)], 3, flags=0x80)
+        dm.dmuon_plan([(4, 4)], 3, flags=0x100)
     assert e.value.status == dm.ERR_UNSUPPORTED
+    for both in (dm.FLAG_PAIR_TILES, dm.FLAG_TUNE):
+        with pytest.raises(dm.DmuonError) as e:
+            dm.dmuon_plan([(4, 4)], 3, flags=dm.FLAG_ONE_SM_TILES | both)
+        assert e.value.status == dm.ERR_INVALID_ARG
 
 
 def test_step_before_bind_is_refused():
@@ -127,9 +131,13 @@ def test_plan_buckets_tiles_and_work(name):
         want[k] = (cnt + 1, tr + (r > c))
     got = {(b["m"], b["n"]): (b["count"], b["transposed"]) for b in d["buckets"]}
     assert got == want
-    # tile counts: upper-triangle tiles for the symmetric products, full grid for the gemm
-    g_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, b["bn_sym"], b["bn_gemm"])[0] for b in d["buckets"])
-    m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], bm, b["bn_sym"], b["bn_gemm"])[1] for b in d["buckets"])
+    # tile counts: upper-triangle tiles for the symmetric products, full grid for the gemm; pair tiles
+    # are 256 rows high
+    def rows(b):
+        return 256 if b["pair"] else bm
+
+    g_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], rows(b), b["bn_sym"], b["bn_gemm"])[0] for b in d["buckets"])
+    m_tot = sum(b["count"] * brute_tiles(b["m"], b["n"], rows(b), b["bn_sym"], b["bn_gemm"])[1] for b in d["buckets"])
     for b in d["buckets"]:
         if w.compute == "bf16":
             # 256-wide tiles unless 1.4x their count exceeds the count of 128-wide ones
@@ -137,6 +145,10 @@ def test_plan_buckets_tiles_and_work(name):
             gemm = {bn: brute_tiles(b["m"], b["n"], bm, bn, bn)[1] for bn in (128, 256)}
             assert b["bn_sym"] == (256 if 1.4 * sym[256] <= sym[128] else 128), b
             assert b["bn_gemm"] == (256 if 1.4 * gemm[256] <= gemm[128] else 128), b
+            # two-SM pairs by default where 256 x 256 tiles fill the short side
+            assert b["pair"] == (b["m"] % 256 == 0 and b["bn_sym"] == b["bn_gemm"] == 256), b
+        else:
+            assert not b["pair"], b
     assert sum(c["gram"] for c in d["lists"]) == g_tot
     assert sum(c["poly"] for c in d["lists"]) == g_tot
     assert sum(c["gemm"] for c in d["lists"]) == m_tot
@@ -266,7 +278,7 @@ def test_workspace_regions_are_disjoint_and_do_not_depend_on_tiling(name):
     has sized the workspace, so nothing may move with them)."""
     w = wl.get(name)
     plans = [dm.dmuon_plan(w.shapes, w.ns_steps, flags=f)
-             for f in (0, dm.FLAG_PAIR_TILES, dm.FLAG_TUNE, dm.FLAG_STATIC_TILES)]
+             for f in (0, dm.FLAG_ONE_SM_TILES, dm.FLAG_TUNE, dm.FLAG_STATIC_TILES)]
     descs = [p.describe() for p in plans]
     for p, d in zip(plans, descs):
         regs = [d["regions"]["status"]] + d["regions"]["tables"] + d["regions"]["scratch"]

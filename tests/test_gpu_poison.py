@@ -101,9 +101,9 @@ def fill(run, seed):
         run.view(run.G, i).copy_(random_matrix(r, c, seed + 2 * i + 1, 1e-3, "cuda", run.param))
 
 
-@pytest.mark.parametrize("form", ["standard", "gram", "pair", "aX", "fp32"])
+@pytest.mark.parametrize("form", ["one_sm", "gram", "pair", "aX", "fp32"])
 def test_poisoned_workspace_ragged_shapes(form):
-    flags = {"standard": 0, "gram": dm.FLAG_GRAM_NS, "pair": dm.FLAG_PAIR_TILES, "aX": dm.FLAG_EPILOGUE_AX,
+    flags = {"one_sm": dm.FLAG_ONE_SM_TILES, "gram": dm.FLAG_GRAM_NS, "pair": 0, "aX": dm.FLAG_EPILOGUE_AX,
              "fp32": 0}[form]
     dt = "f32" if form == "fp32" else "bf16"
     shapes = RAGGED + ([(512, 1024), (1024, 512), (768, 2048)] if form == "pair" else [])
