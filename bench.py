@@ -37,9 +37,9 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
-    "gemm": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
-    "gram": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
-    "poly": ["tc_ns.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
+    "gemm": ["tc_ns.cu", "tc_ns2.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
+    "gram": ["tc_ns.cu", "tc_ns2.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
+    "poly": ["tc_ns.cu", "tc_ns2.cu", "tc_epilogue.cuh", "ptx.cuh", "internal.h"],
     "momentum": ["momentum.cu", "stream_tile.cuh", "internal.h"],
     "norm": ["momentum.cu", "stream_tile.cuh", "internal.h"],
 }
