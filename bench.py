@@ -482,8 +482,9 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
 
 def tuned_buckets(plan):
     """A tuned plan's choice per bucket, with the measured cost (SM-ms per matrix) of each candidate:
-    one-SM 128 wide, one-SM 256 wide, two-SM pairs (0 = not timed)."""
-    return [{k: b[k] for k in ("m", "n", "pair", "bn_sym", "bn_gemm", "tune_cost")} for b in plan.describe()["buckets"]]
+    one-SM 128 wide, one-SM 256 wide, two-SM pairs (0 = not timed), and the gemm's part of it."""
+    return [{k: b[k] for k in ("m", "n", "pair", "bn_sym", "bn_gemm", "tune_cost", "tune_cost_gemm")}
+            for b in plan.describe()["buckets"]]
 
 
 def tile_kinds(plan):

@@ -135,6 +135,7 @@ struct BucketPlan {
   // 0 = not measured
   double tile_ms[3] = {0, 0, 0};
   double tune_cost[3] = {0, 0, 0};  // tuning: SM-ms per matrix of one-SM 128, one-SM 256, pairs (0 = not timed)
+  double tune_gemm[3] = {0, 0, 0};  // the part of tune_cost spent in the gemm
   std::vector<int32_t> mats;  // slot -> global matrix index
   int64_t off_slotmat = -1;
   int64_t off[kBufCount] = {-1, -1, -1, -1, -1, -1, -1};
@@ -910,7 +911,10 @@ dmuon_status tune_plan(dmuon_plan_s& P, cudaStream_t s) {
       add_tiles(P, DMUON_KIND_GEMM, 0, T, tiles);
       cg[ci] = tiles.size() * n_gm * tt.sm_ms[ci][2];
     }
-    for (int ci = 0; ci < kTuneCands; ++ci) B.tune_cost[ci] = cs[ci] + cg[ci] < 1e299 ? cs[ci] + cg[ci] : 0.0;
+    for (int ci = 0; ci < kTuneCands; ++ci) {
+      B.tune_cost[ci] = cs[ci] + cg[ci] < 1e299 ? cs[ci] + cg[ci] : 0.0;
+      B.tune_gemm[ci] = cg[ci] < 1e299 ? cg[ci] : 0.0;
+    }
     // Best one-SM widths, then pairs against them. A configuration other than the planner's default
     // must be cheaper by kTuneMargin: what a probe gains per clock, a long step under the power limit
     // partly gives back in clock (measured: pairs chosen on a 2 % probe advantage lost 5 % on MoE).
@@ -1703,10 +1707,11 @@ dmuon_status dmuon_plan_describe(dmuon_plan_t P, char* buf, size_t len, size_t* 
     snprintf(t, sizeof t,
              "%s{\"m\": %d, \"n\": %d, \"count\": %d, \"transposed\": %d, \"x_ld\": %d, \"m_ld\": %d, "
              "\"form\": \"%s\", \"pair\": %s, \"bn_sym\": %d, \"bn_gemm\": %d, "
-             "\"tile_ms\": [%.6g, %.6g, %.6g], \"tune_cost\": [%.6g, %.6g, %.6g]}",
+             "\"tile_ms\": [%.6g, %.6g, %.6g], \"tune_cost\": [%.6g, %.6g, %.6g], "
+             "\"tune_cost_gemm\": [%.6g, %.6g, %.6g]}",
              b ? ", " : "", B.m, B.n, B.count, B.n_transposed, B.x_ld, B.m_ld, B.gram ? "gram" : "standard",
              B.pair ? "true" : "false", B.bn_sym, B.bn_gemm, B.tile_ms[0], B.tile_ms[1], B.tile_ms[2],
-             B.tune_cost[0], B.tune_cost[1], B.tune_cost[2]);
+             B.tune_cost[0], B.tune_cost[1], B.tune_cost[2], B.tune_gemm[0], B.tune_gemm[1], B.tune_gemm[2]);
     j += t;
   }
   j += "], \"regions\": {";
