@@ -354,14 +354,15 @@ def timed_steps(plan, step, steps, stream, launches_per_step, local, world, barr
     c0 = plan.launch_count()
     torch.cuda.synchronize()
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
         step()
-    ev1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
+    elapsed_ms = ev[0].elapsed_time(ev[-1])
+    timed_steps.last_step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     launches = plan.launch_count() - c0
     prof = plan.profile_end(steps * launches_per_step)
     clk = clocks.stop() if clocks else None
@@ -380,6 +381,40 @@ def timed_steps(plan, step, steps, stream, launches_per_step, local, world, barr
         d["work"] += work
         d["launches"] += 1
     return max_over_ranks(elapsed_ms, world, f"cuda:{local}"), per_kind, launches, status, clk
+
+
+def step_stats(ms_list):
+    """Median, 90th percentile and range of per-step times (ms)."""
+    xs = sorted(ms_list)
+    if not xs:
+        return None
+    p90 = xs[min(len(xs) - 1, int(round(0.9 * (len(xs) - 1))))]
+    return {"median": statistics.median(xs), "p90": p90, "min": xs[0], "max": xs[-1]}
+
+
+def graph_replay(plan_step, stream, steps, warmup):
+    """One step captured in a CUDA graph on ``stream`` and replayed: ``warmup`` untimed replays,
+    then ``steps`` timed ones with an event between every two. Returns per-step ms. The caller
+    has already run the step with the same pointers, so the capture records no host copies."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        plan_step()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            g.replay()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    out = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    del g
+    return out
 
 
 def cta_tails(plan, step, stream):
@@ -470,7 +505,7 @@ def measure_workload(name, args, local, tensor_peak, hbm_peak, alu_peak):
                (ns_tflops / peak) if ns_tflops else None,
            "compute": w.compute, "kernels": kernel_table(per_kind, steps, tensor_peak, hbm_peak, alu_peak, w.compute,
                                                          w.name),
-           "ms_by_ns_step": timed_steps.last_by_step,
+           "ms_by_ns_step": timed_steps.last_by_step, "step_ms": step_stats(timed_steps.last_step_ms),
            **({"tuned_buckets": tuned_buckets(plan)} if args.tune else {}),
            "gpu_launches": launches, "device_status": status, "clocks": clk,
            "cta_tails": cta_tails(plan, step, stream) if w.compute == "bf16" else None}
@@ -589,7 +624,15 @@ def run_ours(args):
                 "work_per_launch": d["work"] / d["launches"], "ms_per_launch": d["ms"] / d["launches"],
                 "traffic": traffic_for(dom, w.name)}
     kernels = kernel_table(per_kind, args.steps, tensor_peak, hbm_peak, alu_peak, w.compute, w.name)
+    step_ms = step_stats(timed_steps.last_step_ms)
     tails = cta_tails(plan, step, stream) if w.compute == "bf16" else None
+
+    # ---- the same step captured once in a CUDA graph and replayed (no host work per step)
+    graph = None
+    if not args.no_graph:
+        g_ms = graph_replay(step, stream, args.steps, args.warmup)
+        graph = {"ms_per_step": sum(g_ms) / len(g_ms), **step_stats(g_ms), "steps": len(g_ms),
+                 "device_status": plan.read_device_status(sh)}
 
     # ---- the Gram-space form of the iteration on the same matrix set (reported beside the headline):
     # its speed-up over the standard form, and the throughput of the flops it actually executes
@@ -780,6 +823,7 @@ def run_ours(args):
         "matrices_per_s": tot["matrices"] * world * args.steps / (max_ms * 1e-3),
         "ns_ms_per_step": ns_ms, "ns_tflops": ns_tflops,
         "ns_frac_of_sustained_peak": ns_tflops / tensor_peak if ns_tflops else None,
+        "step_ms": step_ms, "graph_replay": graph,
         "kernels": kernels, "ms_by_ns_step": ms_by_ns_step, "cta_tails": tails, "roofline": roof, "gram_form": gram, "cpu_baseline": cpu, "e2e": e2e,
         "per_workload": per_workload,
         **({"adamw_other_params": adamw} if adamw is not None else {}),
@@ -813,6 +857,7 @@ def main(argv=None):
     ap.add_argument("--one-sm", action="store_true",
                     help="one-SM tiles everywhere instead of 256 x 256 tiles on CTA pairs where they fit")
     ap.add_argument("--static-tiles", action="store_true", help="deal tiles round-robin instead of claiming them")
+    ap.add_argument("--no-graph", action="store_true", help="leave out the CUDA-graph replay timing")
     ap.add_argument("--tune", action="store_true", help="choose tile configurations by timing them at bind")
     ap.add_argument("--adamw", action="store_true",
                     help="also time the AdamW kernel over Llama-3.1-8B's non-matrix parameters")

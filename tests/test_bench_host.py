@@ -1,7 +1,7 @@
 """Host-side pieces of bench.py that need no GPU: the kernel fingerprint that
 ties the committed DRAM-traffic figures to the kernel code they were taken
-on (so that they read null once the code changes), and the bench's JSON
-contract for the reference arm."""
+on (so that they read null once the code changes), the per-step statistics,
+and the bench's JSON contract for the reference arm."""
 
 import json
 import subprocess
@@ -20,6 +20,13 @@ def test_fingerprint_ignores_comments_but_not_code():
 
 def test_traffic_is_null_for_unknown_workloads():
     assert bench.traffic_for("gemm", "no-such-workload") is None
+
+
+def test_step_stats():
+    st = bench.step_stats([5.0, 1.0, 4.0, 2.0, 3.0, 10.0, 6.0, 7.0, 8.0, 9.0, 11.0])
+    assert st == {"median": 6.0, "p90": 10.0, "min": 1.0, "max": 11.0}
+    assert bench.step_stats([]) is None
+    assert bench.step_stats([2.5]) == {"median": 2.5, "p90": 2.5, "min": 2.5, "max": 2.5}
 
 
 def test_reference_arm_line():
