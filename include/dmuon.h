@@ -92,16 +92,17 @@ typedef struct {
                                           Space Recurrence"). Fewer flops when the
                                           matrix is wide (>= 26% fewer at 2:1);
                                           others keep the standard form.          */
-#define DMUON_FLAG_PAIR_TILES 0x8u    /* the default, accepted for callers that set
-                                          it: buckets whose short side is a multiple
-                                          of 256 and whose products run 256 wide use
-                                          256 x 256 tiles on pairs of SMs (two-SM
+#define DMUON_FLAG_PAIR_TILES 0x8u    /* 256 x 256 tiles on pairs of SMs (two-SM
                                           UMMA, thread-block clusters of 2; bf16
-                                          only), other buckets one-SM tiles. Test
-                                          hook: with the environment variable
-                                          DMUON_TEST_FORCE_PAIRS=1, every bucket
-                                          with a short side >= 256 gets pairs (as
-                                          DMUON_FLAG_TUNE may choose).           */
+                                          only) for every bucket whose short side
+                                          is a multiple of 256 and whose products
+                                          run 256 wide. Without the flag the same
+                                          holds for short sides of at least 1024
+                                          (the default); other buckets use one-SM
+                                          tiles. Test hook: with the environment
+                                          variable DMUON_TEST_FORCE_PAIRS=1, every
+                                          bucket with a short side >= 256 gets
+                                          pairs (as DMUON_FLAG_TUNE may choose).  */
 #define DMUON_FLAG_EPILOGUE_AX 0x10u   /* standard form: add the a*X_k term of the
                                           quintic step in the epilogue of the
                                           product B X_k (reading the X_k tile),

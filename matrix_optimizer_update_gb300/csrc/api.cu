@@ -274,6 +274,9 @@ int dtype_bytes(int32_t d) { return d == DMUON_BF16 ? 2 : 4; }
 // is the default unless its tiles, weighted by 1.4, outnumber those of 128.
 constexpr double kWideTileCost = 1.4;
 
+// Shortest short side that gets two-SM pair tiles by default.
+constexpr int kPairMinShort = 1024;
+
 // Tiles of a symmetric m x m product: row block ti (bm rows) covers columns
 // from its diagonal block on, ti*bm + tj*bn for tj = 0, 1, ..., so no tile
 // reaches below the diagonal block of its rows.
@@ -345,13 +348,18 @@ dmuon_status build_plan(dmuon_plan_s& P) {
     P.buckets[b].gram = (P.flags & DMUON_FLAG_GRAM_NS) && P.ns_steps >= 1 && order[b].second >= 2 * order[b].first;
     P.buckets[b].bn_sym = P.tc ? default_bn_sym(order[b].first) : kSimtBN;
     P.buckets[b].bn_gemm = P.tc ? default_bn_gemm(order[b].second) : kSimtBN;
-    // two-SM 256 x 256 tiles (the default) where both dimensions fill them: no 256-row tile is left
-    // half empty (tuning may still choose them for other short sides >= 256, and so does the test hook)
+    // two-SM 256 x 256 tiles (the default) where they fill the short side, so that no 256-row tile is
+    // left half empty, and where it spans at least 4 row pairs: below that the diagonal pair tiles,
+    // half of whose work lies below the diagonal, weigh too much (measured by tuning: short sides of
+    // 256 and 512 run 9-12 % faster on one-SM tiles, 1024 level, 1536 and up faster on pairs).
+    // DMUON_FLAG_PAIR_TILES asks for them on shorter sides too. Tuning may still choose pairs for
+    // other short sides >= 256, and so does the test hook.
     const bool pairs_on = P.tc && !(P.flags & DMUON_FLAG_ONE_SM_TILES);
     const bool forced = pairs_on && order[b].first >= 256 && test_hook_env("DMUON_TEST_FORCE_PAIRS");
+    const bool long_enough = order[b].first >= kPairMinShort || (P.flags & DMUON_FLAG_PAIR_TILES);
     if (forced) P.buckets[b].bn_sym = P.buckets[b].bn_gemm = 256;
-    P.buckets[b].pair = forced || (pairs_on && order[b].first % 256 == 0 && P.buckets[b].bn_sym == 256 &&
-                                   P.buckets[b].bn_gemm == 256);
+    P.buckets[b].pair = forced || (pairs_on && order[b].first % 256 == 0 && long_enough &&
+                                   P.buckets[b].bn_sym == 256 && P.buckets[b].bn_gemm == 256);
   }
 
   P.mats.assign(n_mats, MatDev{});

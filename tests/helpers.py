@@ -62,8 +62,8 @@ class LibRun:
 
     def __init__(self, shapes, *, param="bf16", grad="bf16", compute="bf16", ns_steps=5, coeffs=ref.DEFAULT_COEFFS,
                  eps=1e-7, capture=True, device="cuda", gram_ns=False, pair=None, epilogue_ax=False, flags=0):
-        # pair: None = the library's default (two-SM tiles where they fill the short side), True = the
-        # same asked for explicitly, False = one-SM tiles everywhere
+        # pair: None = the library's default (two-SM tiles where they fill a short side of at least
+        # 1024), True = two-SM tiles wherever they fill the short side, False = one-SM tiles everywhere
         self.shapes = list(shapes)
         self.param, self.grad, self.compute = param, grad, compute
         self.offs, total = layout(self.shapes)

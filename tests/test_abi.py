@@ -145,8 +145,8 @@ def test_plan_buckets_tiles_and_work(name):
             gemm = {bn: brute_tiles(b["m"], b["n"], bm, bn, bn)[1] for bn in (128, 256)}
             assert b["bn_sym"] == (256 if 1.4 * sym[256] <= sym[128] else 128), b
             assert b["bn_gemm"] == (256 if 1.4 * gemm[256] <= gemm[128] else 128), b
-            # two-SM pairs by default where 256 x 256 tiles fill the short side
-            assert b["pair"] == (b["m"] % 256 == 0 and b["bn_sym"] == b["bn_gemm"] == 256), b
+            # two-SM pairs by default where 256 x 256 tiles fill a short side of at least 1024
+            assert b["pair"] == (b["m"] % 256 == 0 and b["m"] >= 1024 and b["bn_sym"] == b["bn_gemm"] == 256), b
         else:
             assert not b["pair"], b
     assert sum(c["gram"] for c in d["lists"]) == g_tot
