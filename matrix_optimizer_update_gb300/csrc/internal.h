@@ -22,7 +22,7 @@ constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2
 // fp32 SIMT tile.
 constexpr int kSimtBM = 64;
 constexpr int kSimtBN = 64;
-constexpr int kSimtBK = 16;
+constexpr int kSimtBK = 64;  // K staged 64 at a time: few rounds of loads and barriers on short K
 constexpr int kSimtThreads = 256;
 
 // Streaming unit of the momentum pass: 8192 contiguous elements (flat mode)

@@ -5,7 +5,8 @@
 // W update fused into the last step), computed with fp32 FFMA on CUDA cores:
 // TF32 tensor math keeps only 10 mantissa bits and cannot reach fp32-level
 // agreement. One 64 x 64 output tile per CTA, 256 threads, 4 x 4 outputs per
-// thread, K staged 16 at a time through shared memory.
+// thread, K staged 64 at a time through shared memory (each thread still sums
+// over K in increasing order, so the stage depth does not change the result).
 #include <cuda_bf16.h>
 
 #include "internal.h"
