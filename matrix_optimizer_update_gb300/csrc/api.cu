@@ -30,6 +30,7 @@
 
 #include "dmuon.h"
 #include "internal.h"
+#include "simt.h"
 
 using namespace dmuon;
 

@@ -19,12 +19,6 @@ constexpr int kTcBN = 256;  // default tile width
 constexpr int kTcBK = 64;
 constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..9 epilogue
 
-// fp32 SIMT tile.
-constexpr int kSimtBM = 64;
-constexpr int kSimtBN = 64;
-constexpr int kSimtBK = 64;  // K staged 64 at a time: few rounds of loads and barriers on short K
-constexpr int kSimtThreads = 256;
-
 // Streaming unit of the momentum pass: 8192 contiguous elements (flat mode)
 // or a 64 x 128 tile of the stored matrix (tiled mode).
 constexpr int kFlatUnit = 8192;
@@ -110,32 +104,6 @@ struct TcParams {
 
 constexpr int kMaxCtaRecords = 1024;  // CTAs per launch the per-CTA profiling records
 
-// One bucket as seen by a fp32 SIMT launch.
-struct SimtBucket {
-  const int32_t* slot_mat;
-  const float* opA;   // gram: X (m x n); poly: A (m x m); gemm: B (m x m)
-  const float* opB;   // gram: X; poly: A; gemm: X_k
-  float* out;
-  const float* aux;
-  int64_t a_mat_stride, b_mat_stride, out_mat_stride, aux_mat_stride;  // elements
-  int32_t a_ld, b_ld, out_ld, aux_ld;
-  int32_t m, n, kdim, pad;
-};
-
-struct SimtParams {
-  SimtBucket bk[kMaxBucketsPerLaunch];
-  const int4* items;
-  int32_t n_items;
-  int32_t first, last;
-  float a, b, c, lr;
-  float diag;  // poly phase: added on the diagonal
-  const MatDev* mats;
-  const uint64_t* ptrs;
-  const float* s_norm;
-  float* capture;
-  int32_t param_bf16;
-};
-
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_momentum(const StreamParams& p, int grid, cudaStream_t s);
 cudaError_t launch_norm_finalize(const StreamParams& p, int grid, cudaStream_t s);
@@ -144,7 +112,6 @@ int momentum_blocks_per_sm(int grad_bf16, int x_bf16);  // resident CTAs per SM 
 cudaError_t launch_tc(int phase, int bn, const TcParams& p, int grid, cudaStream_t s);
 // Two-SM form: 256 x 256 tiles on clusters of two CTAs; `pairs` clusters.
 cudaError_t launch_tc_pair(int phase, const TcParams& p, int pairs, cudaStream_t s);
-cudaError_t launch_simt(int phase, const SimtParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(unsigned* status, int64_t limit_ns, cudaStream_t s);
 // status word -> mapped host word (device address of it), then cleared
 cudaError_t launch_status_readout(unsigned* status, unsigned* host_out_dev, cudaStream_t s);

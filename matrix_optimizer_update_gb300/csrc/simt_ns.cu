@@ -4,12 +4,13 @@
 // with mirrored stores; poly B = b*A + c*A A^T; gemm X' = a*X + B X with the
 // W update fused into the last step), computed with fp32 FFMA on CUDA cores:
 // TF32 tensor math keeps only 10 mantissa bits and cannot reach fp32-level
-// agreement. One 64 x 64 output tile per CTA, 256 threads, 4 x 4 outputs per
-// thread, K staged 64 at a time through shared memory (each thread still sums
-// over K in increasing order, so the stage depth does not change the result).
+// agreement. One kSimtBM x kSimtBN output tile per CTA, 256 threads in a 16 x 16
+// grid, each with (kSimtBM / 16) x (kSimtBN / 16) outputs, K staged kSimtBK at a
+// time through shared memory. Each output is summed over K in increasing order
+// by one thread, so neither the tile shape nor the stage depth changes the result.
 #include <cuda_bf16.h>
 
-#include "internal.h"
+#include "simt.h"
 
 namespace dmuon {
 namespace {
@@ -25,17 +26,18 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
   const int row0 = it.z * kSimtBM, col0 = (PHASE == kPhaseGemm) ? it.w * kSimtBN : row0 + it.w * kSimtBN;
   const float* opA = B.opA + slot * B.a_mat_stride;
   const float* opB = B.opB + slot * B.b_mat_stride;
+  constexpr int TM = kSimtBM / 16, TN = kSimtBN / 16;  // outputs per thread along rows / columns
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int m = B.m, kdim = B.kdim;
   // output columns are bounded by m (gram/poly) or n (gemm)
   const int ncols = (PHASE == kPhaseGemm) ? B.n : B.m;
 
-  float acc[4][4];
+  float acc[TM][TN];
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < TM; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+    for (int c = 0; c < TN; ++c) acc[r][c] = 0.f;
 
   for (int k0 = 0; k0 < kdim; k0 += kSimtBK) {
     // A operand rows row0.., K contiguous in memory
@@ -62,15 +64,15 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kSimtBK; ++k) {
-      float a[4], b[4];
+      float a[TM], b[TN];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = As[k][ty * 4 + r];
+      for (int r = 0; r < TM; ++r) a[r] = As[k][ty * TM + r];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) b[c] = Bs[k][tx * 4 + c];
+      for (int c = 0; c < TN; ++c) b[c] = Bs[k][tx * TN + c];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < TM; ++r)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+        for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
     }
     __syncthreads();
   }
@@ -85,12 +87,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
   float* out = B.out ? B.out + slot * B.out_mat_stride : nullptr;
   const float* aux = B.aux ? B.aux + slot * B.aux_mat_stride : nullptr;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = row0 + ty * 4 + r;
+  for (int r = 0; r < TM; ++r) {
+    const int i = row0 + ty * TM + r;
     if (i >= m) continue;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int j = col0 + tx * 4 + c;
+    for (int c = 0; c < TN; ++c) {
+      const int j = col0 + tx * TN + c;
       if (j >= ncols) continue;
       float v = acc[r][c];
       if (PHASE == kPhaseGram || PHASE == kPhasePoly) {

@@ -157,7 +157,7 @@ def test_plan_buckets_tiles_and_work(name):
     # every launch of a chunk shares the chunk's tile widths
     assert [L["kind"] for L in d["launches"][:2]] == [dm.KIND_MOMENTUM, dm.KIND_NORM]
     for L in d["launches"][2:]:
-        assert L["bn"] in ((128, 256) if w.compute == "bf16" else (64,))
+        assert L["bn"] in ((128, 256) if w.compute == "bf16" else (32,))  # fp32: 32 x 32 SIMT tiles
     work = {}
     for L in d["launches"]:
         work[L["kind"]] = work.get(L["kind"], 0.0) + L["work"]
