@@ -12,6 +12,7 @@ constexpr int kSimtBM = 32;
 constexpr int kSimtBN = 32;
 constexpr int kSimtBK = 64;
 constexpr int kSimtThreads = 256;
+constexpr int kSimtGroup = 4;  // K stages whose loads a thread issues together (K up to 256 at once)
 
 // One bucket as seen by a fp32 SIMT launch.
 struct SimtBucket {

@@ -39,42 +39,70 @@ __global__ void __launch_bounds__(kSimtThreads) simt_ns_kernel(const __grid_cons
 #pragma unroll
     for (int c = 0; c < TN; ++c) acc[r][c] = 0.f;
 
-  for (int k0 = 0; k0 < kdim; k0 += kSimtBK) {
-    // A operand rows row0.., K contiguous in memory
-    for (int e = tid; e < kSimtBM * kSimtBK; e += kSimtThreads) {
-      const int r = e / kSimtBK, k = e % kSimtBK;
-      const int gr = row0 + r, gk = k0 + k;
-      As[k][r] = (gr < m && gk < kdim) ? opA[(int64_t)gr * B.a_ld + gk] : 0.f;
-    }
+  // Operand elements this thread moves per K stage, and the stages whose loads are issued together:
+  // the loads of up to kSimtGroup stages go out at once into registers, so a short K waits on memory
+  // about once; each stage then passes through shared memory in turn.
+  constexpr int kPerA = kSimtBM * kSimtBK / kSimtThreads, kPerB = kSimtBN * kSimtBK / kSimtThreads;
+  static_assert(kPerA * kSimtThreads == kSimtBM * kSimtBK && kPerB * kSimtThreads == kSimtBN * kSimtBK,
+                "tiles must split evenly over the threads");
+  // A operand element e of a stage: row e / BK, k e % BK (rows of opA, K contiguous in memory).
+  auto load_a = [&](int k0, int q) -> float {
+    const int e = tid + q * kSimtThreads;
+    const int gr = row0 + e / kSimtBK, gk = k0 + e % kSimtBK;
+    return (gr < m && gk < kdim) ? opA[(int64_t)gr * B.a_ld + gk] : 0.f;
+  };
+  // B operand element e: gemm, X_k row k (K) e / BN, column e % BN (columns contiguous in memory);
+  // symmetric products, row col0 + e / BK of the same matrix, k e % BK.
+  auto load_b = [&](int k0, int q) -> float {
+    const int e = tid + q * kSimtThreads;
     if (PHASE == kPhaseGemm) {
-      // B operand = X_k rows k (K), columns col0.. contiguous in memory
-      for (int e = tid; e < kSimtBN * kSimtBK; e += kSimtThreads) {
-        const int k = e / kSimtBN, c = e % kSimtBN;
-        const int gk = k0 + k, gc = col0 + c;
-        Bs[k][c] = (gk < kdim && gc < ncols) ? opB[(int64_t)gk * B.b_ld + gc] : 0.f;
-      }
-    } else {
-      // B operand = rows col0.. of the same matrix (the product with its transpose)
-      for (int e = tid; e < kSimtBN * kSimtBK; e += kSimtThreads) {
-        const int c = e / kSimtBK, k = e % kSimtBK;
-        const int gc = col0 + c, gk = k0 + k;
-        Bs[k][c] = (gc < ncols && gk < kdim) ? opB[(int64_t)gc * B.b_ld + gk] : 0.f;
-      }
+      const int gk = k0 + e / kSimtBN, gc = col0 + e % kSimtBN;
+      return (gk < kdim && gc < ncols) ? opB[(int64_t)gk * B.b_ld + gc] : 0.f;
     }
-    __syncthreads();
+    const int gc = col0 + e / kSimtBK, gk = k0 + e % kSimtBK;
+    return (gc < ncols && gk < kdim) ? opB[(int64_t)gc * B.b_ld + gk] : 0.f;
+  };
+  for (int g0 = 0; g0 < kdim; g0 += kSimtGroup * kSimtBK) {
+    float ra[kSimtGroup][kPerA], rb[kSimtGroup][kPerB];
 #pragma unroll
-    for (int k = 0; k < kSimtBK; ++k) {
-      float a[TM], b[TN];
+    for (int st = 0; st < kSimtGroup; ++st) {
+      const int k0 = g0 + st * kSimtBK;
 #pragma unroll
-      for (int r = 0; r < TM; ++r) a[r] = As[k][ty * TM + r];
+      for (int q = 0; q < kPerA; ++q) ra[st][q] = (k0 < kdim) ? load_a(k0, q) : 0.f;
 #pragma unroll
-      for (int c = 0; c < TN; ++c) b[c] = Bs[k][tx * TN + c];
-#pragma unroll
-      for (int r = 0; r < TM; ++r)
-#pragma unroll
-        for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+      for (int q = 0; q < kPerB; ++q) rb[st][q] = (k0 < kdim) ? load_b(k0, q) : 0.f;
     }
-    __syncthreads();
+#pragma unroll
+    for (int st = 0; st < kSimtGroup; ++st) {
+      if (g0 + st * kSimtBK >= kdim) break;
+#pragma unroll
+      for (int q = 0; q < kPerA; ++q) {
+        const int e = tid + q * kSimtThreads;
+        As[e % kSimtBK][e / kSimtBK] = ra[st][q];
+      }
+#pragma unroll
+      for (int q = 0; q < kPerB; ++q) {
+        const int e = tid + q * kSimtThreads;
+        if (PHASE == kPhaseGemm)
+          Bs[e / kSimtBN][e % kSimtBN] = rb[st][q];
+        else
+          Bs[e % kSimtBK][e / kSimtBK] = rb[st][q];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kSimtBK; ++k) {
+        float a[TM], b[TN];
+#pragma unroll
+        for (int r = 0; r < TM; ++r) a[r] = As[k][ty * TM + r];
+#pragma unroll
+        for (int c = 0; c < TN; ++c) b[c] = Bs[k][tx * TN + c];
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+          for (int c = 0; c < TN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+      }
+      __syncthreads();
+    }
   }
 
   const int gm = B.slot_mat[slot];
