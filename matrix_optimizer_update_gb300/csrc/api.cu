@@ -8,9 +8,11 @@
 // ("DMuon: Efficient Distributed Muon Training with Near-Adam Overhead",
 // gist.science summary section 2, "Batching": batch matrices of similar shape
 // and run the recurrence jointly to amortise dispatch). Within a launch the
-// tiles are sorted by cost, largest first, and dealt round-robin to the
-// persistent CTAs: the greedy fallback of the cost-based balancing of
-// section 2.3, applied to SMs instead of owner ranks.
+// tiles are sorted by cost, largest first, and each persistent CTA (or CTA
+// pair) claims the next one from a counter when it becomes free: list
+// scheduling in cost order, the greedy makespan balancing of section 2.3
+// applied to SMs instead of owner ranks (DMUON_FLAG_STATIC_TILES deals the
+// same list round-robin instead).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
