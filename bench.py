@@ -853,7 +853,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gram", action="store_true", help="skip the Gram-space form measurement")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other matrix sets")
-    ap.add_argument("--per-workload-steps", type=int, default=5, help="timed steps per other matrix set")
+    ap.add_argument("--per-workload-steps", type=int, default=10, help="timed steps per other matrix set")
     ap.add_argument("--one-sm", action="store_true",
                     help="one-SM tiles everywhere instead of 256 x 256 tiles on CTA pairs where they fit")
     ap.add_argument("--static-tiles", action="store_true", help="deal tiles round-robin instead of claiming them")
